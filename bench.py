@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Throughput of the fused attention forward on one GB300 (or N, as replicas).
+
+A step is one pass of the hot path over one batch: the non-causal and the
+causal forward of the headline workload (B=1, H=32, N=4096, d=128, bf16 Q/K/V
+i.i.d. N(0,1), scale 1/sqrt(d)).  FLOPs are counted as 4*B*H*N^2*d for the
+non-causal pass and half that for the causal one.  Inputs are resident in
+device memory when timing starts; L2 is flushed (a 256 MiB write) before
+every step, outside the per-step CUDA events.  The JSON line also carries the
+roofline of the dominant kernel, the fp64 oracle timed on the host as a CPU
+baseline, an end-to-end figure through host buffers, clocks sampled with
+nvidia-smi, and the number of kernels launched.
+
+--impl reference times the oracle itself on the host (bounded samples of the
+same workload); under torchrun only rank 0 does so.
+"""
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_20_gb300.inputs import HEADLINE, WORKLOADS, make_qkv  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (bf16, causal/non-causal) N=4096 d=128; % of GB300 BF16 peak"
+KERNEL_SOURCES = [
+    os.path.join(ROOT, "exact_attention_20_gb300", "csrc", n)
+    for n in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh", "fa_api.cu")
+]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+FLUSH_BYTES = 256 << 20
+
+
+def flops(w, causal):
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    return f / 2 if causal else f
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained"), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def recorded_traffic(workload, causal):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel sources changed since those counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("bytes_per_launch", {}).get(f"{workload}:{'causal' if causal else 'non-causal'}")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        # samples inside the timed region (second resolution), else the last
+        # second of warm-up before it
+        inside = [r for r in rows if self.t0 - 1 <= r[0] <= self.t1 + 1]
+        use = inside or rows
+        mhz = sorted(r[1] for r in use)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region +-1 s" if inside else "whole run"}
+
+
+def dist_setup(n_gpus):
+    if n_gpus <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank, world = int(os.environ["RANK"]), int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, n_heads, seed=0):
+    """Runs the fp64 oracle on n_heads heads of the workload, both masks;
+    returns (TFLOP/s on the sample, seconds, description)."""
+    import numpy as np
+
+    import oracle
+
+    q, k, v = make_qkv(1, n_heads, w.N, w.d, seed=seed, values=w.values)
+    qf, kf, vf = (t.float().numpy().astype(np.float64) for t in (q, k, v))
+    t0 = time.perf_counter()
+    for causal in (False, True):
+        oracle.attention(qf, kf, vf, w.scale, causal)
+    dt = time.perf_counter() - t0
+    fl = sum(4.0 * n_heads * w.N * w.N * w.d / (2 if c else 1) for c in (False, True))
+    desc = f"{n_heads} of {w.B * w.H} heads of {w.name}, non-causal and causal, fp64 numpy"
+    return fl / dt / 1e12, dt, desc
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, 1)
+    times, rates = [], []
+    desc = ""
+    for i in range(args.steps):
+        r, dt, desc = oracle_sample_rate(w, 1, seed=i)
+        rates.append(r)
+        times.append(dt)
+    fl = sum(4.0 * w.N * w.N * w.d / (2 if c else 1) for c in (False, True))
+    value = fl * len(times) / sum(times) / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "masks": ["non-causal", "causal"], "sample": "1 head per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc + " per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    from exact_attention_20_gb300 import build as fa_build
+
+    rank, world, local = dist_setup(args.gpus)
+    if rank == 0 or world == 1:
+        fa_build.build()
+    barrier(world)
+    from exact_attention_20_gb300 import fa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    masks = [c for c in (False, True) if c in w.causal]
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, seed=1234 + rank, values=w.values, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        for i, causal in enumerate(masks):
+            if evs is not None:
+                evs[i][0].record(stream)
+            fa.fa_fwd(q, k, v, o, lse, causal=causal, scale=w.scale, stream=stream)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    # warm-up: at least args.warmup steps and at least one second of work
+    t_warm = time.time()
+    n = 0
+    while n < args.warmup or time.time() - t_warm < 1.0:
+        flush.zero_()
+        step()
+        n += 1
+        if n % 8 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+            for _ in masks] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.mark("t0")
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        step(evs[s])
+    torch.cuda.synchronize(dev)
+    wall1 = time.perf_counter()
+    sampler.mark("t1")
+    barrier(world)
+    per_mask_ms = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)]
+                   for i in range(len(masks))]
+    step_ms = sum(sum(x) for x in per_mask_ms) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    step_flops = sum(flops(w, c) for c in masks)
+    value = world * step_flops / (step_ms * 1e-3) / 1e12
+
+    # end to end through the public API from pinned host buffers
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = [torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in masks]
+    lh = [torch.empty(lse.shape, dtype=torch.float32, pin_memory=True) for _ in masks]
+    ws = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+    def e2e_step():
+        for t_d, t_h in zip(ws, (qh, kh, vh)):
+            t_d.copy_(t_h, non_blocking=True)
+        for i, causal in enumerate(masks):
+            fa.fa_fwd(ws[0], ws[1], ws[2], o, lse, causal=causal, scale=w.scale, stream=stream)
+            oh[i].copy_(o, non_blocking=True)
+            lh[i].copy_(lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e_steps = max(3, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(e_steps):
+        flush.zero_()
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = sum(t.numel() * t.element_size() for t in oh + lh)
+
+    clocks = sampler.stop()
+    if rank != 0:
+        return
+
+    peak_burst, peak_sustained, peak_kind = measured_peaks()
+    dom = 0  # the non-causal launch carries two thirds of the step
+    dom_ms = sum(per_mask_ms[dom]) / args.steps
+    achieved = flops(w, masks[dom]) / (dom_ms * 1e-3) / 1e12
+    per_mask = {}
+    for i, c in enumerate(masks):
+        ms = sum(per_mask_ms[i]) / args.steps
+        tf = flops(w, c) / (ms * 1e-3) / 1e12
+        per_mask["causal" if c else "non-causal"] = {
+            "ms": ms, "tflops": tf, "frac_of_measured_peak": tf / peak_burst}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, dt, desc = oracle_sample_rate(w, args.cpu_heads)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{desc}; {dt:.1f} s; BLAS products on all cores, elementwise steps single-threaded"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "masks": ["causal" if c else "non-causal" for c in masks],
+                   "scale": w.scale, "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_mask": per_mask,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                     "peak_kind": f"{peak_kind} bf16 dense, burst",
+                     "kernel": f"fa_fwd_kernel<{w.d},{str(masks[dom]).lower()}>",
+                     "traffic": recorded_traffic(w.name, masks[dom])},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * len(masks),
+        "clocks": clocks,
+        "wall_s_timed_region": wall1 - wall0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-heads", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

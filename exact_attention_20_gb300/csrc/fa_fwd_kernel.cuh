@@ -1,0 +1,528 @@
+// Fused exact attention forward for sm_103a: one persistent CTA per SM, each
+// work item = two adjacent 128-row query tiles of one (batch, head).
+//
+// The method is the FlashAttention-2 forward ("FlashAttention and kernels.",
+// sections "From a sum to an output row" and "FlashAttention's forward pass";
+// "Kernels and FlashAttention: When the Same Math Runs 7.6x Faster",
+// section 2.8): query tiles outer, key/value tiles inner, running row maximum
+// m, running row sum l and an unnormalised fp32 accumulator rescaled by
+// alpha = exp(m_old - m_new), divided by l once at the end, plus the per-row
+// logsumexp.  Exponentials are taken in base 2 with the softmax scale folded
+// into one FMA, m kept in log2 units and L converted back with ln 2 ("How to
+// profile and optimise kernels", Round 4, "exp2").  Key tiles above the
+// diagonal are never visited; only the diagonal tile and a ragged last tile
+// are masked (same article, Round 4, "Causal tile-skipping").
+//
+// GB300 mapping (warp specialisation, FlashAttention-3's idea of separate
+// load and math warps carried over to tcgen05):
+//   warps 0-3  softmax warpgroup for query tile 0 (one row per thread)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q tiles once per item, then K_j, V_j into a ring
+//   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j on
+//              the tensor core, accumulators in tensor memory; owns TMEM.
+// Tensor memory (512 columns x 128 lanes, fp32): S_0 at column 0, S_1 at 128,
+// O_0 at 256, O_1 at 384.  P_t (bf16, two per column) overwrites the first
+// 64 columns of S_t and is the A operand of the P.V product.  While one
+// warpgroup exponentiates, the tensor core works on the other query tile.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBlockM = 128;                 // query rows per tile
+constexpr int kBlockN = 128;                 // keys per K/V tile
+constexpr int kQTiles = 2;                   // query tiles per work item
+constexpr int kItemRows = kBlockM * kQTiles; // query rows per work item
+constexpr int kSlabBytes = 128 * 64 * 2;     // one 128-row x 64-column bf16 TMA box
+constexpr int kNumThreads = 320;
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+// Codes recorded in the device status word when a wait gives up.
+constexpr int kSiteProducer = 1;
+constexpr int kSiteMma = 2;
+constexpr int kSiteSoftmax = 3;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+  static constexpr int kTileBytes = (D / 64) * kSlabBytes;         // one 128 x D bf16 tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;               // K/V ring depth (tiles)
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
+  static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2]
+  //           o_done[2] o_free[2] drain[1]
+  static constexpr int kNumBars = 2 * 2 + 2 * kStages + 2 * 4 + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;           // + alignment slack
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;        // [BH][N][D]
+  float* lse;              // [BH][N]
+  int* status;             // device status word (0 = ok)
+  int N;
+  int BH;
+  int n_key_tiles;         // ceil(N / 128)
+  int n_row_blocks;        // ceil(N / 256)
+  int num_items;           // BH * n_row_blocks
+  float qk_scale;          // scale * log2(e)
+  unsigned long long wait_limit_ns;
+  int starve_kv;           // watchdog self-test: the producer never delivers K/V
+};
+
+// Work item -> (row block, batch*head).  Heads vary fastest; row blocks run
+// from the last to the first, so under the causal mask the longest items
+// start first ("How to profile and optimise kernels", Round 5: reversed
+// query-tile order, heads on the fast axis).
+__device__ __forceinline__ void decode_item(int item, const FwdParams& p, int& rb, int& bh) {
+  bh = item % p.BH;
+  rb = p.n_row_blocks - 1 - item / p.BH;
+}
+
+// Number of key tiles query tile t of row block rb visits (0 if the tile
+// lies beyond N).
+template <bool CAUSAL>
+__device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
+  const int r0 = rb * kItemRows + t * kBlockM;
+  if (r0 >= p.N) return 0;
+  if (CAUSAL) return min(r0 / kBlockN + 1, p.n_key_tiles);
+  return p.n_key_tiles;
+}
+
+struct Sync {
+  uint32_t q_full[2], q_empty[2], s_full[2], p_ready[2], o_done[2], o_free[2], drain;
+  uint32_t kv_full0, kv_empty0;  // arrays of kStages barriers, 8 bytes apart
+  volatile int* abort_flag;
+};
+
+// Bounded wait: true when the phase completed; false if this CTA is aborting
+// or the wait ran past the limit (then the failure is recorded).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Sync& sy,
+                                           const FwdParams& p, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t polls = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++polls & 31u) == 0u) {
+      if (*sy.abort_flag) return false;
+      if (global_timer_ns() - t0 > p.wait_limit_ns) {
+        *sy.abort_flag = 1;
+        atomicCAS(p.status, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             uint32_t sbase, const Sync& sy, const FwdParams& p) {
+  using C = Cfg<D>;
+  uint32_t q_loads[2] = {0, 0};
+  uint32_t kv_count = 0;
+  const uint64_t pol_q = l2_policy_evict_first();
+  const uint64_t pol_kv = l2_policy_evict_last();
+  bool ok = true;
+  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+    int rb, bh;
+    decode_item(item, p, rb, bh);
+    const int n0 = tiles_for<CAUSAL>(rb, 0, p);
+    const int n1 = tiles_for<CAUSAL>(rb, 1, p);
+    const int nkv = max(n0, n1);
+    for (int t = 0; t < kQTiles && ok; ++t) {
+      if ((t == 0 ? n0 : n1) == 0) continue;
+      ok = wait_phase(sy.q_empty[t], (q_loads[t] & 1u) ^ 1u, sy, p, kSiteProducer);
+      if (!ok) break;
+      ++q_loads[t];
+      mbar_arrive_expect_tx(sy.q_full[t], C::kTileBytes);
+      const uint32_t dst = sbase + C::kQOff + t * C::kTileBytes;
+      const int row = rb * kItemRows + t * kBlockM;
+#pragma unroll
+      for (int s = 0; s < D / 64; ++s)
+        tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * 64, row, bh, pol_q);
+    }
+    if (p.starve_kv) continue;  // self-test: never deliver K/V
+    for (int j = 0; j < nkv && ok; ++j) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t slot = kv_count % C::kStages;
+        const uint32_t par = ((kv_count / C::kStages) & 1u) ^ 1u;
+        ok = wait_phase(sy.kv_empty0 + 8 * slot, par, sy, p, kSiteProducer);
+        if (!ok) break;
+        const uint32_t full = sy.kv_full0 + 8 * slot;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        const uint32_t dst = sbase + C::kKVOff + slot * C::kTileBytes;
+        const CUtensorMap* map = which == 0 ? tmK : tmV;
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_3d_hint(dst + s * kSlabBytes, map, full, s * 64, j * kBlockN, bh, pol_kv);
+        ++kv_count;
+      }
+    }
+  }
+  // Drain: wait until every copy this thread started has landed, so none is
+  // still writing shared memory when the CTA exits (also after an abort).
+  // These waits ignore the abort flag: copies in flight land whatever happened.
+  const uint32_t first = kv_count > (uint32_t)C::kStages ? kv_count - C::kStages : 0;
+  for (uint32_t c = first; c < kv_count; ++c)
+    mbar_wait_bounded(sy.kv_full0 + 8 * (c % C::kStages), (c / C::kStages) & 1u, p.wait_limit_ns);
+  for (int t = 0; t < kQTiles; ++t)
+    if (q_loads[t] > 0) mbar_wait_bounded(sy.q_full[t], (q_loads[t] - 1) & 1u, p.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    // 16 columns of d per instruction; 4 steps per 64-column swizzled slab
+    const uint32_t off = (kk / 4) * kSlabBytes + (kk % 4) * 32;
+    umma_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
+            kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+                                         bool accumulate) {
+  // V is [keys][d] with d contiguous: an MN-major B operand.  16 keys per
+  // instruction = two 8-row swizzle groups (2048 bytes); the two 64-column
+  // slabs of d = 128 are 16 KB apart (leading byte offset).
+  constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
+#pragma unroll
+  for (int kk = 0; kk < kBlockN / 16; ++kk) {
+    umma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, kSlabBytes, 1024), idesc,
+            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool CAUSAL>
+__device__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy, const FwdParams& p) {
+  using C = Cfg<D>;
+  uint32_t q_uses[2] = {0, 0};
+  uint32_t kv_count = 0;
+  uint32_t pr_par[2] = {0, 0};
+  uint32_t of_par[2] = {1, 1};
+  bool ok = true;
+  auto kv_slot_ready = [&](uint32_t c) -> uint32_t {
+    const uint32_t slot = c % C::kStages;
+    ok = ok && wait_phase(sy.kv_full0 + 8 * slot, (c / C::kStages) & 1u, sy, p, kSiteMma);
+    return slot;
+  };
+  auto q_addr = [&](int t) { return sbase + C::kQOff + t * C::kTileBytes; };
+  auto kv_addr = [&](uint32_t slot) { return sbase + C::kKVOff + slot * C::kTileBytes; };
+  auto tm_s = [&](int t) { return tmem + t * 128; };
+  auto tm_o = [&](int t) { return tmem + 256 + t * 128; };
+
+  // O_t += P_t V for the item's key tile jv (first tile overwrites O_t).
+  auto pv_step = [&](int t, int jv, uint32_t vslot) {
+    ok = ok && wait_phase(sy.p_ready[t], pr_par[t], sy, p, kSiteMma);
+    pr_par[t] ^= 1u;
+    if (jv == 0) {
+      ok = ok && wait_phase(sy.o_free[t], of_par[t], sy, p, kSiteMma);
+      of_par[t] ^= 1u;
+    }
+    if (!ok) return;
+    tc_fence_after_sync();
+    issue_pv<D>(tm_o(t), tm_s(t), kv_addr(vslot), jv > 0);
+    umma_commit(sy.o_done[t]);
+  };
+
+  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+    int rb, bh;
+    decode_item(item, p, rb, bh);
+    const int n[2] = {tiles_for<CAUSAL>(rb, 0, p), tiles_for<CAUSAL>(rb, 1, p)};
+    const int nkv = max(n[0], n[1]);
+    for (int t = 0; t < kQTiles; ++t) {
+      if (n[t] == 0) continue;
+      ok = ok && wait_phase(sy.q_full[t], q_uses[t] & 1u, sy, p, kSiteMma);
+      ++q_uses[t];
+    }
+    // key tile 0: S_0 and S_1
+    {
+      const uint32_t ks = kv_slot_ready(kv_count);
+      if (!ok) break;
+      tc_fence_after_sync();
+      for (int t = 0; t < kQTiles; ++t) {
+        if (n[t] == 0) continue;
+        issue_qk<D>(tm_s(t), q_addr(t), kv_addr(ks));
+        umma_commit(sy.s_full[t]);
+        if (n[t] == 1) umma_commit(sy.q_empty[t]);
+      }
+      umma_commit(sy.kv_empty0 + 8 * ks);
+    }
+    for (int j = 1; j <= nkv && ok; ++j) {
+      const int jv = j - 1;                                   // value tile of this step
+      const uint32_t vs = kv_slot_ready(kv_count + 2 * jv + 1);
+      const bool have_k = j < nkv;
+      const uint32_t ks = have_k ? kv_slot_ready(kv_count + 2 * j) : 0u;
+      if (!ok) break;
+      if (jv < n[0]) pv_step(0, jv, vs);
+      if (ok && have_k && j < n[0]) {
+        issue_qk<D>(tm_s(0), q_addr(0), kv_addr(ks));
+        umma_commit(sy.s_full[0]);
+        if (j == n[0] - 1) umma_commit(sy.q_empty[0]);
+      }
+      if (ok && jv < n[1]) pv_step(1, jv, vs);
+      if (!ok) break;
+      umma_commit(sy.kv_empty0 + 8 * vs);
+      if (have_k) {
+        if (j < n[1]) {
+          issue_qk<D>(tm_s(1), q_addr(1), kv_addr(ks));
+          umma_commit(sy.s_full[1]);
+          if (j == n[1] - 1) umma_commit(sy.q_empty[1]);
+        }
+        umma_commit(sy.kv_empty0 + 8 * ks);
+      }
+    }
+    kv_count += 2 * nkv;
+  }
+  // Every MMA issued so far must finish before tensor memory is released.
+  umma_commit(sy.drain);
+  mbar_wait_bounded(sy.drain, 0, p.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax / correction / epilogue warpgroup (128 threads, one row each)
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParams& p) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
+  const int row_in_tile = quad * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t tS = tmem + lane_off + t * 128;
+  const uint32_t tO = tmem + lane_off + 256 + t * 128;
+  const float qk = p.qk_scale;
+  const bool ragged = (p.N % kBlockN) != 0;
+  uint32_t s_par = 0, o_par = 0;
+  bool ok = true;
+
+  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+    int rb, bh;
+    decode_item(item, p, rb, bh);
+    const int n = tiles_for<CAUSAL>(rb, t, p);
+    if (n == 0) continue;
+    const int row = rb * kItemRows + t * kBlockM + row_in_tile;
+    float m = -INFINITY;  // running maximum, log2 units (already times qk_scale)
+    float l = 0.f;        // running sum of exp2(s*qk - m), for the logsumexp
+    float lq = 0.f;       // running sum of the same terms rounded to bf16, for O
+
+    for (int j = 0; j < n; ++j) {
+      ok = wait_phase(sy.s_full[t], s_par, sy, p, kSiteSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      s_par ^= 1u;
+      tc_fence_after_sync();
+
+      uint32_t s[128];
+      tmem_ld32_wait(tS + 0, &s[0]);
+      tmem_ld32_wait(tS + 32, &s[32]);
+      tmem_ld32_wait(tS + 64, &s[64]);
+      tmem_ld32_wait(tS + 96, &s[96]);
+
+      // Mask the diagonal tile (causal) and the ragged last tile: a key is
+      // kept iff key <= min(row, N-1) (causal) or key <= N-1.
+      const bool need_mask = (CAUSAL && j == n - 1) || (ragged && j == p.n_key_tiles - 1);
+      if (need_mask) {
+        const int lim = (CAUSAL ? min(row, p.N - 1) : p.N - 1) - j * kBlockN;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) s[c] = __float_as_uint(-INFINITY);
+      }
+
+      float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+      float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(s[c]));
+        mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float m_new = fmaxf(m, mx * qk);          // qk > 0, so max commutes with the scale
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);      // 0 on the first tile, 1 if the max held
+      const float neg_m = -m_use;
+
+      float rs0 = 0.f, rs1 = 0.f, rq0 = 0.f, rq1 = 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = ex2_approx(fmaf(__uint_as_float(s[c4 * 32 + 2 * i]), qk, neg_m));
+          const float b = ex2_approx(fmaf(__uint_as_float(s[c4 * 32 + 2 * i + 1]), qk, neg_m));
+          pk[i] = pack_bf16x2(a, b);
+          rs0 += a;
+          rs1 += b;
+          // also sum the bf16 values the P.V product multiplies, so that
+          // O / lq is an exact weighted average of the value rows
+          rq0 += __uint_as_float(pk[i] << 16);
+          rq1 += __uint_as_float(pk[i] & 0xFFFF0000u);
+        }
+        tmem_st16(tS + c4 * 16, pk);
+      }
+      l = l * alpha + (rs0 + rs1);
+      lq = lq * alpha + (rq0 + rq1);
+
+      if (j > 0) {
+        // O_t holds the sum up to tile j-1; rescale it to the new maximum.
+        ok = wait_phase(sy.o_done[t], o_par, sy, p, kSiteSoftmax);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        o_par ^= 1u;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_wait(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(sy.p_ready[t]);
+      m = m_new;
+    }
+    if (!ok) break;
+
+    // Epilogue: wait for the last P.V, then O = O_acc / l in bf16 and the
+    // natural-log logsumexp L = (m + log2 l) * ln 2.
+    ok = wait_phase(sy.o_done[t], o_par, sy, p, kSiteSoftmax);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    o_par ^= 1u;
+    tc_fence_after_sync();
+    const float inv_l = 1.f / lq;
+    const bool store = row < p.N;
+    __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32_wait(tO + c * 32, o);
+      uint4 pk[4];
+      uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (store) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+      }
+    }
+    if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+    tc_fence_before_sync();
+    mbar_arrive(sy.o_free[t]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Kernel
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kNumThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  Sync sy;
+  {
+    uint32_t b = sbase + C::kBarOff;
+    for (int t = 0; t < 2; ++t) sy.q_full[t] = b + 8 * t;
+    b += 16;
+    for (int t = 0; t < 2; ++t) sy.q_empty[t] = b + 8 * t;
+    b += 16;
+    sy.kv_full0 = b;
+    b += 8 * C::kStages;
+    sy.kv_empty0 = b;
+    b += 8 * C::kStages;
+    for (int t = 0; t < 2; ++t) sy.s_full[t] = b + 8 * t;
+    b += 16;
+    for (int t = 0; t < 2; ++t) sy.p_ready[t] = b + 8 * t;
+    b += 16;
+    for (int t = 0; t < 2; ++t) sy.o_done[t] = b + 8 * t;
+    b += 16;
+    for (int t = 0; t < 2; ++t) sy.o_free[t] = b + 8 * t;
+    b += 16;
+    sy.drain = b;
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sy.q_full[t], 1);
+      mbar_init(sy.q_empty[t], 1);
+      mbar_init(sy.s_full[t], 1);
+      mbar_init(sy.p_ready[t], kBlockM);
+      mbar_init(sy.o_done[t], 1);
+      mbar_init(sy.o_free[t], kBlockM);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(sy.kv_full0 + 8 * s, 1);
+      mbar_init(sy.kv_empty0 + 8 * s, 1);
+    }
+    mbar_init(sy.drain, 1);
+    *sy.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) run_mma<D, CAUSAL>(sbase, tmem, sy, p);
+    __syncwarp();
+  } else {
+    run_softmax<D, CAUSAL>(warp >> 2, tmem, sy, p);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

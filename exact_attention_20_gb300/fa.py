@@ -1,0 +1,173 @@
+"""Thin ctypes binding of libfa_gb300.so: argument marshalling only.
+
+Every step of the attention forward runs in the CUDA library; this module
+checks tensor metadata, passes raw device pointers and sizes through the C
+ABI declared in include/fa_gb300.h, and turns status codes into exceptions.
+There is no CPU fallback: without the built library, or on a device other
+than a GB300, every compute call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_NULL = -2
+FA_ERR_ALIGN = -3
+FA_ERR_ALIAS = -4
+FA_ERR_DEVICE = -5
+FA_ERR_LAUNCH = -6
+FA_ERR_DEVICE_TIMEOUT = -7
+
+# every function declared in include/fa_gb300.h, with its ctypes signature
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_get_device_status": (_I, [_P]),
+    "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
+    "fa_version": (_I, []),
+}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(strerror(code) if _lib is not None else f"fa status {code}")
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the CUDA library (once); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; build it with `python -m exact_attention_20_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().fa_strerror(int(code)).decode()
+
+
+def version() -> int:
+    return lib().fa_version()
+
+
+def fa_fwd_raw(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int,
+               causal: int, scale: float, stream: int = 0) -> int:
+    """Direct call of the C entry point with integer addresses; returns the status code."""
+    return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stream)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(name, t, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None) -> None:
+    """O and LSE into caller-owned tensors. q, k, v, o: bf16 [B, H, N, d]; lse: fp32 [B, H, N]."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check(name, t, torch.bfloat16, (B, H, N, d), dev)
+    _check("lse", lse, torch.float32, (B, H, N), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocates O (bf16) and LSE (fp32) next to q and runs the forward; returns (O, LSE)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
+    return o, lse
+
+
+def attention_host(q, k, v, causal: bool = False, scale: float | None = None, device="cuda",
+                   stream=None, out=None, workspace=None):
+    """End-to-end call from host memory: copies q, k, v (pinned host bf16) to the
+    device, runs the forward, and copies O and LSE back into host tensors.
+
+    ``workspace`` may hold preallocated device tensors (q, k, v, o, lse) and
+    ``out`` preallocated pinned host tensors (o, lse), so that repeated calls
+    allocate nothing.  Returns (o_host, lse_host); synchronises the stream.
+    """
+    dev = torch.device(device)
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = tuple(torch.empty_like(t, device=dev) for t in (q, k, v)) + (
+            torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev),
+            torch.empty((B, H, N), dtype=torch.float32, device=dev))
+    qd, kd, vd, od, lsed = workspace
+    if out is None:
+        out = (torch.empty((B, H, N, d), dtype=torch.bfloat16, pin_memory=True),
+               torch.empty((B, H, N), dtype=torch.float32, pin_memory=True))
+    oh, lseh = out
+    s = torch.cuda.current_stream(dev) if stream is None else stream
+    with torch.cuda.stream(s):
+        qd.copy_(q, non_blocking=True)
+        kd.copy_(k, non_blocking=True)
+        vd.copy_(v, non_blocking=True)
+        fa_fwd(qd, kd, vd, od, lsed, causal=causal, scale=scale, stream=s)
+        oh.copy_(od, non_blocking=True)
+        lseh.copy_(lsed, non_blocking=True)
+    s.synchronize()
+    return oh, lseh
+
+
+def device_status(stream=None) -> int:
+    """FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up on a wait (clears the record)."""
+    return lib().fa_get_device_status(_stream_handle(stream))
+
+
+def watchdog_selftest(limit_ms: int = 100, device="cuda") -> int:
+    """Runs the deliberate-starvation self-test; returns the status the library reports."""
+    dev = torch.device(device)
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device=dev)
+    k, v, o = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        return lib().fa_watchdog_selftest(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                          lse.data_ptr(), int(limit_ms),
+                                          torch.cuda.current_stream(dev).cuda_stream)

@@ -1,0 +1,100 @@
+/*
+ * fa_gb300.h — C ABI of the GB300 (sm_103a) fused exact attention forward.
+ *
+ * The operation.  For every batch b, head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * Q[b,h,i,:] . K[b,h,j,:] ) * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp( scale * Q[b,h,i,:] . K[b,h,j,:] )
+ *
+ * where j runs over 0..N-1, or over 0..i when causal (top-left mask, key j
+ * visible to query i iff j <= i).  This is Eq. 4.1 of "4 Triton and Custom
+ * Kernels" (aisyseng.dev, section 4.7), with the logsumexp output of
+ * "FlashAttention 2 from PyTorch to Triton" (section "What I am building")
+ * and "FlashAttention and kernels." (section "FlashAttention's forward pass").
+ * The kernel computes it tile by tile with the online softmax (running row
+ * maximum, running row sum, rescaled fp32 accumulator, exp2), so the N x N
+ * score matrix never reaches device memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named q, k, v, o, lse are DEVICE pointers on the current device.
+ *     The caller owns every buffer; nothing is allocated per call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream) and return a status code.
+ *   - Status 0 is FA_OK.  A negative status is returned for an error found
+ *     before launch; nothing is launched and the outputs are left untouched.
+ *     No entry point aborts, throws or prints.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,    /* B, H or N < 1; d not 64 or 128; causal not 0/1;
+                                 scale not finite or <= 0; sizes overflowing indices */
+  FA_ERR_NULL = -2,           /* a required pointer is NULL */
+  FA_ERR_ALIGN = -3,          /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+  FA_ERR_ALIAS = -4,          /* o or lse overlaps an input, or o overlaps lse */
+  FA_ERR_DEVICE = -5,         /* current device is not compute capability 10.3 (sm_103a) */
+  FA_ERR_LAUNCH = -6,         /* a CUDA call failed (tensor-map encoding, attribute, launch) */
+  FA_ERR_DEVICE_TIMEOUT = -7  /* a pipeline wait inside the kernel gave up (see fa_get_device_status) */
+};
+
+/*
+ * fa_fwd — fused attention forward.
+ *
+ *   q, k, v : bf16 [B][H][N][d], contiguous (d fastest), read only.
+ *   o       : bf16 [B][H][N][d], contiguous; written.  Must not overlap q, k, v or lse.
+ *   lse     : fp32 [B][H][N]; written with the natural-log logsumexp of each
+ *             row of scaled (and masked) scores.
+ *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 1,
+ *             with B*H*N*d < 2^31.
+ *   d       : head dimension, 64 or 128.
+ *   causal  : 0 = every key visible; 1 = key j visible to query i iff j <= i.
+ *   scale   : multiplies Q.K before the softmax (typically 1/sqrt(d)); finite, > 0.
+ *   stream  : cudaStream_t as void*.
+ *
+ * P (the softmax numerators) is rounded to bf16 before the P.V product and O
+ * is rounded once to bf16 (round to nearest even) after the fp32 division by
+ * the row sum ("How to profile and optimise kernels", the cast of P to bf16).
+ * Returns FA_OK or a negative fa_status.  Rows i >= N are never written.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/* Human-readable name of a status code; never NULL, static storage. */
+const char* fa_strerror(int code);
+
+/*
+ * fa_get_device_status — reports whether any kernel launched by this library
+ * on the current device gave up on a pipeline wait (every wait inside the
+ * kernel is bounded in time; on expiry the kernel records the failure, stops
+ * its pipeline, releases tensor memory and exits instead of hanging).
+ * Synchronises `stream`, returns FA_OK or FA_ERR_DEVICE_TIMEOUT, and clears
+ * the recorded state.  Returns FA_ERR_LAUNCH if the status cannot be read.
+ */
+int fa_get_device_status(void* stream);
+
+/*
+ * fa_watchdog_selftest — launches one small forward whose load warp is told
+ * never to deliver its K/V tiles, with every wait limited to `limit_ms`
+ * milliseconds, so that the bounded waits run out on purpose.  q, k, v, o
+ * and lse are as for fa_fwd with B=H=1, N=128, d=64 (caller-owned, device).
+ * Synchronises `stream` and returns what fa_get_device_status then reports
+ * (FA_ERR_DEVICE_TIMEOUT when the watchdog works), or a launch error.
+ * Test hook for the failure-detection path; never used by fa_fwd.
+ */
+int fa_watchdog_selftest(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int limit_ms, void* stream);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

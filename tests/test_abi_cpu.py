@@ -1,0 +1,111 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol,
+and rejects bad arguments before touching CUDA (no compute call here)."""
+import os
+import re
+
+import pytest
+import torch
+
+from exact_attention_20_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    fa_build.build()
+    from exact_attention_20_gb300 import fa as mod
+    mod.lib()
+    return mod
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert names == ["fa_fwd", "fa_get_device_status", "fa_strerror", "fa_version",
+                     "fa_watchdog_selftest"]
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = fa.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(fa.SIGNATURES)
+
+
+def test_version_and_strerror(fa):
+    assert fa.version() == 100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        msg = fa.strerror(code)
+        assert msg.startswith("FA_")
+    assert fa.strerror(12345) == "unknown fa status code"
+
+
+# Fake, 256-byte aligned, far-apart addresses: every call below fails its host
+# checks before any CUDA call, so nothing is dereferenced.
+A = 1 << 40
+STEP = 1 << 36
+Q, K, V, O, L = (A + i * STEP for i in range(5))
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,scale", [
+    (0, 1, 128, 64, 0, 0.125), (1, 0, 128, 64, 0, 0.125), (1, 1, 0, 64, 0, 0.125),
+    (1, 1, -5, 64, 0, 0.125), (1, 1, 128, 32, 0, 0.125), (1, 1, 128, 96, 0, 0.125),
+    (1, 1, 128, 256, 0, 0.125), (1, 1, 128, 64, 2, 0.125), (1, 1, 128, 64, -1, 0.125),
+    (1, 1, 128, 64, 0, 0.0), (1, 1, 128, 64, 0, -0.5), (1, 1, 128, 64, 0, float("inf")),
+    (1, 1, 128, 64, 0, float("nan")), (1 << 12, 1 << 12, 1 << 10, 128, 0, 0.1),
+])
+def test_invalid_arguments(fa, B, H, N, d, causal, scale):
+    assert fa.fa_fwd_raw(Q, K, V, O, L, B, H, N, d, causal, scale) == fa.FA_ERR_INVALID_ARG
+
+
+def test_null_pointers(fa):
+    for i in range(5):
+        ptrs = [Q, K, V, O, L]
+        ptrs[i] = 0
+        assert fa.fa_fwd_raw(*ptrs, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_NULL
+
+
+def test_misaligned_pointers(fa):
+    for i in range(4):
+        ptrs = [Q, K, V, O, L]
+        ptrs[i] += 8
+        assert fa.fa_fwd_raw(*ptrs, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIGN
+    assert fa.fa_fwd_raw(Q, K, V, O, L + 2, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIGN
+
+
+def test_aliasing_outputs(fa):
+    nbytes = 1 * 2 * 256 * 64 * 2
+    assert fa.fa_fwd_raw(Q, K, V, Q, L, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
+    assert fa.fa_fwd_raw(Q, K, V, K + nbytes - 16, L, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
+    assert fa.fa_fwd_raw(Q, K, V, O, V + 64, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
+    assert fa.fa_fwd_raw(Q, K, V, O, O + nbytes - 4, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
+    # touching but not overlapping is fine for the host checks (then no device here)
+    rc = fa.fa_fwd_raw(Q, K, V, Q + nbytes, L, 1, 2, 256, 64, 0, 0.125)
+    assert rc != fa.FA_ERR_ALIAS
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
+def test_valid_call_without_a_device_fails_loudly(fa):
+    rc = fa.fa_fwd_raw(Q, K, V, O, L, 1, 2, 256, 64, 0, 0.125)
+    assert rc in (fa.FA_ERR_LAUNCH, fa.FA_ERR_DEVICE)
+
+
+def test_binding_refuses_cpu_tensors(fa):
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.attention(q, q, q)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="CPU-only check")
+def test_binding_has_no_cpu_fallback(fa, monkeypatch):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "LIB_PATH", "/nonexistent/libfa_gb300.so")
+    with pytest.raises(RuntimeError):
+        fa.lib()
