@@ -240,11 +240,12 @@ def run_ours(args):
                 evs[i][1].record(stream)
 
     sampler = ClockSampler(local)
-    sampler.start()
-    # warm-up: at least args.warmup steps and at least one second of work
+    if not args.quick:
+        sampler.start()
+    # warm-up: at least args.warmup steps and (unless --quick) one second of work
     t_warm = time.time()
     n = 0
-    while n < args.warmup or time.time() - t_warm < 1.0:
+    while n < args.warmup or (not args.quick and time.time() - t_warm < 1.0):
         flush.zero_()
         step()
         n += 1
@@ -271,6 +272,11 @@ def run_ours(args):
     step_ms = max_over_ranks(step_ms, world)
     step_flops = sum(flops(w, c) for c in masks)
     value = world * step_flops / (step_ms * 1e-3) / 1e12
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"quick": True, "workload": w.name, "ms_per_step": step_ms,
+                              "value": value, "unit": "TFLOP/s"}), flush=True)
+        return
 
     # end to end through the public API from pinned host buffers
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
@@ -359,6 +365,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-heads", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the timed kernel steps (for profiler runs): no clock sampling, "
+                         "no end-to-end leg, no CPU baseline, no one-second warm-up floor")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

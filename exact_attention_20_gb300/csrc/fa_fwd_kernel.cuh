@@ -41,6 +41,9 @@ constexpr int kNumThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
+// The reference maximum moves only when a tile's maximum exceeds it by more
+// than this many log2 units (so exponentials stay <= 2^8 = 256).
+constexpr float kRescaleThreshold = 8.0f;
 
 // Codes recorded in the device status word when a wait gives up.
 constexpr int kSiteProducer = 1;
@@ -318,9 +321,15 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
     const int n = tiles_for<CAUSAL>(rb, t, p);
     if (n == 0) continue;
     const int row = rb * kItemRows + t * kBlockM + row_in_tile;
-    float m = -INFINITY;  // running maximum, log2 units (already times qk_scale)
-    float l = 0.f;        // running sum of exp2(s*qk - m), for the logsumexp
-    float lq = 0.f;       // running sum of the same terms rounded to bf16, for O
+    // m_ref: the reference maximum the exponentials are taken against (log2
+    // units, already times qk_scale).  It is moved only when a tile's maximum
+    // exceeds it by more than kRescaleThreshold, so P = exp2(s*qk - m_ref) may
+    // reach 2^kRescaleThreshold.  l, lq and O all use the same m_ref, so the
+    // shift cancels in O = acc / lq and in L = m_ref + log2 l exactly as in the
+    // every-tile update ("Softmax, the safe way": a common shift factors out).
+    float m_ref = -INFINITY;
+    float l = 0.f;        // running sum of exp2(s*qk - m_ref), for the logsumexp
+    float lq = 0.f;       // the same terms rounded to bf16 (what P.V multiplies), for O
 
     for (int j = 0; j < n; ++j) {
       ok = wait_phase(sy.s_full[t], s_par, sy, p, kSiteSoftmax);
@@ -330,10 +339,7 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
       tc_fence_after_sync();
 
       uint32_t s[128];
-      tmem_ld32_wait(tS + 0, &s[0]);
-      tmem_ld32_wait(tS + 32, &s[32]);
-      tmem_ld32_wait(tS + 64, &s[64]);
-      tmem_ld32_wait(tS + 96, &s[96]);
+      tmem_ld128_wait(tS, s);
 
       // Mask the diagonal tile (causal) and the ragged last tile: a key is
       // kept iff key <= min(row, N-1) (causal) or key <= N-1.
@@ -345,64 +351,88 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
           if (c > lim) s[c] = __float_as_uint(-INFINITY);
       }
 
-      float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-      float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+      // row maximum: four independent chains of 32 columns each
+      float mx[4];
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-        mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t* sc = s + 32 * q4;
+        mx[q4] = fmax3(__uint_as_float(sc[0]), __uint_as_float(sc[1]), __uint_as_float(sc[2]));
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      const float m_new = fmaxf(m, mx * qk);          // qk > 0, so max commutes with the scale
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);      // 0 on the first tile, 1 if the max held
-      const float neg_m = -m_use;
+#pragma unroll
+      for (int i = 3; i < 31; i += 2) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          mx[q4] = fmax3(mx[q4], __uint_as_float(s[32 * q4 + i]), __uint_as_float(s[32 * q4 + i + 1]));
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) mx[q4] = fmaxf(mx[q4], __uint_as_float(s[32 * q4 + 31]));
+      const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * qk;  // qk > 0: max commutes with the scale
+      float alpha = 1.f;
+      if (m_tile > m_ref + kRescaleThreshold) {  // always taken on the first tile (m_ref = -inf)
+        alpha = ex2_approx(m_ref - m_tile);      // 0 when m_ref = -inf
+        m_ref = m_tile;
+        l *= alpha;
+        lq *= alpha;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      const uint64_t qk2 = f2_pack(qk, qk);
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
 
-      float rs0 = 0.f, rs1 = 0.f, rq0 = 0.f, rq1 = 0.f;
+      uint64_t sum2 = f2_pack(0.f, 0.f), sumq2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = ex2_approx(fmaf(__uint_as_float(s[c4 * 32 + 2 * i]), qk, neg_m));
-          const float b = ex2_approx(fmaf(__uint_as_float(s[c4 * 32 + 2 * i + 1]), qk, neg_m));
+          const int c = c4 * 32 + 2 * i;
+          const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
+          float xa, xb;
+          f2_unpack(x, xa, xb);
+          const float a = ex2_approx(xa);
+          const float b = ex2_approx(xb);
           pk[i] = pack_bf16x2(a, b);
-          rs0 += a;
-          rs1 += b;
+          sum2 = f2_add(sum2, f2_pack(a, b));
           // also sum the bf16 values the P.V product multiplies, so that
           // O / lq is an exact weighted average of the value rows
-          rq0 += __uint_as_float(pk[i] << 16);
-          rq1 += __uint_as_float(pk[i] & 0xFFFF0000u);
+          sumq2 = f2_add(sumq2, f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
         }
         tmem_st16(tS + c4 * 16, pk);
       }
-      l = l * alpha + (rs0 + rs1);
-      lq = lq * alpha + (rq0 + rq1);
+      float sa, sb, qa, qb;
+      f2_unpack(sum2, sa, sb);
+      f2_unpack(sumq2, qa, qb);
+      l += sa + sb;
+      lq += qa + qb;
 
       if (j > 0) {
-        // O_t holds the sum up to tile j-1; rescale it to the new maximum.
+        // O_t holds the sum up to tile j-1; bring it to the new reference
+        // maximum where a row moved it (alpha = 1 elsewhere, exact).
         ok = wait_phase(sy.o_done[t], o_par, sy, p, kSiteSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         o_par ^= 1u;
         tc_fence_after_sync();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32_wait(tO + c * 32, o);
+          for (int c = 0; c < D / 64; ++c) {
+            uint32_t o[64];
+            tmem_ld64_wait(tO + c * 64, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tO + c * 32, o);
+            for (int i = 0; i < 32; ++i) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), a2), lo, hi);
+              o[2 * i] = __float_as_uint(lo);
+              o[2 * i + 1] = __float_as_uint(hi);
+            }
+            tmem_st32(tO + c * 64, o);
+            tmem_st32(tO + c * 64 + 32, o + 32);
           }
         }
       }
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(sy.p_ready[t]);
-      m = m_new;
     }
     if (!ok) break;
 
@@ -422,16 +452,20 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
       tmem_ld32_wait(tO + c * 32, o);
       uint4 pk[4];
       uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+      const uint64_t il2 = f2_pack(inv_l, inv_l);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      for (int i = 0; i < 16; ++i) {
+        float lo, hi;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2), lo, hi);
+        w[i] = pack_bf16x2(lo, hi);
+      }
       if (store) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = pk[i];
       }
     }
-    if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+    if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     tc_fence_before_sync();
     mbar_arrive(sy.o_free[t]);
   }

@@ -30,8 +30,9 @@ def test_one_ulp_flip_below_four_passes_only_near_a_midpoint():
     # 2.0078 sits near the midpoint of 2.0 and 2.015625: either neighbour is fine
     ref = _ref([2.0078])
     assert_close(compare(_bf16([2.0]), torch.zeros(1), ref, np.zeros(1)))
-    # 2.003 is far from the midpoint: the far neighbour is a real error of 0.0126
-    ref = _ref([2.003])
+    # 2.0005 is far from the midpoint: returning the far neighbour is 0.0146
+    # worse than the nearest bf16 value
+    ref = _ref([2.0005])
     with pytest.raises(AssertionError):
         assert_close(compare(_bf16([2.015625]), torch.zeros(1), ref, np.zeros(1)))
 
