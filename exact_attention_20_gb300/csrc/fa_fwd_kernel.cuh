@@ -20,6 +20,7 @@
 //   warp  8    TMA producer: Q tiles once per item, then K_j, V_j into a ring
 //   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j on
 //              the tensor core, accumulators in tensor memory; owns TMEM.
+//   warps 10-11 idle (they complete the third warpgroup, which setmaxnreg needs)
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 at column 0, S_1 at 128,
 // O_0 at 256, O_1 at 384.  P_t (bf16, two per column) overwrites the first
 // 64 columns of S_t and is the A operand of the P.V product.  While one
@@ -37,9 +38,15 @@ constexpr int kBlockN = 128;                 // keys per K/V tile
 constexpr int kQTiles = 2;                   // query tiles per work item
 constexpr int kItemRows = kBlockM * kQTiles; // query rows per work item
 constexpr int kSlabBytes = 128 * 64 * 2;     // one 128-row x 64-column bf16 TMA box
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 384;             // three warpgroups
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split: the launch gives every thread 168 (65536 / 384, rounded
+// down to 8); the load/MMA warpgroup drops to 104 and the two softmax
+// warpgroups rise to 192: 128*104 + 256*192 = 62464 <= 384*168.
+constexpr uint32_t kRegsAux = 104;
+constexpr uint32_t kRegsSoftmax = 192;
+static_assert(128 * kRegsAux + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds the launch");
 constexpr uint32_t kTmemCols = 512;
 // The reference maximum moves only when a tile's maximum exceeds it by more
 // than this many log2 units (so exponentials stay <= 2^8 = 256).
@@ -128,7 +135,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
-__device__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+__device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              uint32_t sbase, const Sync& sy, const FwdParams& p) {
   using C = Cfg<D>;
   uint32_t q_loads[2] = {0, 0};
@@ -213,7 +220,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 }
 
 template <int D, bool CAUSAL>
-__device__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy, const FwdParams& p) {
+__device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy, const FwdParams& p) {
   using C = Cfg<D>;
   uint32_t q_uses[2] = {0, 0};
   uint32_t kv_count = 0;
@@ -302,7 +309,7 @@ __device__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy, const Fwd
 // Softmax / correction / epilogue warpgroup (128 threads, one row each)
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
-__device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParams& p) {
+__device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParams& p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quad = warp & 3;                       // TMEM lanes 32*quad .. 32*quad+31
@@ -312,6 +319,11 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
   const uint32_t tO = tmem + lane_off + 256 + t * 128;
   const float qk = p.qk_scale;
   const bool ragged = (p.N % kBlockN) != 0;
+  // this warpgroup's barriers, selected once (no run-time array indexing)
+  const uint32_t bar_s_full = t ? sy.s_full[1] : sy.s_full[0];
+  const uint32_t bar_p_ready = t ? sy.p_ready[1] : sy.p_ready[0];
+  const uint32_t bar_o_done = t ? sy.o_done[1] : sy.o_done[0];
+  const uint32_t bar_o_free = t ? sy.o_free[1] : sy.o_free[0];
   uint32_t s_par = 0, o_par = 0;
   bool ok = true;
 
@@ -332,7 +344,7 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
     float lq = 0.f;       // the same terms rounded to bf16 (what P.V multiplies), for O
 
     for (int j = 0; j < n; ++j) {
-      ok = wait_phase(sy.s_full[t], s_par, sy, p, kSiteSoftmax);
+      ok = wait_phase(bar_s_full, s_par, sy, p, kSiteSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       s_par ^= 1u;
@@ -407,7 +419,7 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
       if (j > 0) {
         // O_t holds the sum up to tile j-1; bring it to the new reference
         // maximum where a row moved it (alpha = 1 elsewhere, exact).
-        ok = wait_phase(sy.o_done[t], o_par, sy, p, kSiteSoftmax);
+        ok = wait_phase(bar_o_done, o_par, sy, p, kSiteSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         o_par ^= 1u;
@@ -432,13 +444,13 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(sy.p_ready[t]);
+      mbar_arrive(bar_p_ready);
     }
     if (!ok) break;
 
     // Epilogue: wait for the last P.V, then O = O_acc / l in bf16 and the
     // natural-log logsumexp L = (m + log2 l) * ln 2.
-    ok = wait_phase(sy.o_done[t], o_par, sy, p, kSiteSoftmax);
+    ok = wait_phase(bar_o_done, o_par, sy, p, kSiteSoftmax);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     o_par ^= 1u;
@@ -450,8 +462,7 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
       tmem_ld32_wait(tO + c * 32, o);
-      uint4 pk[4];
-      uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+      uint32_t w[16];
       const uint64_t il2 = f2_pack(inv_l, inv_l);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -462,12 +473,12 @@ __device__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParam
       if (store) {
         uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
     if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     tc_fence_before_sync();
-    mbar_arrive(sy.o_free[t]);
+    mbar_arrive(bar_o_free);
   }
 }
 
@@ -541,13 +552,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kLoadWarp) {
-    if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma<D, CAUSAL>(sbase, tmem, sy, p);
-    __syncwarp();
+  if (warp >= 8) {
+    setmaxnreg_dec<kRegsAux>();
+    if (warp == kLoadWarp) {
+      if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) run_mma<D, CAUSAL>(sbase, tmem, sy, p);
+      __syncwarp();
+    }
   } else {
+    setmaxnreg_inc<kRegsSoftmax>();
     run_softmax<D, CAUSAL>(warp >> 2, tmem, sy, p);
   }
 
