@@ -61,7 +61,7 @@ template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
   static constexpr int kTileBytes = (D / 64) * kSlabBytes;         // one 128 x D bf16 tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;               // K/V ring depth (tiles)
+  static constexpr int kStages = (D == 128) ? 5 : 9;               // K/V ring depth (tiles)
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -193,30 +193,30 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread)
 // ---------------------------------------------------------------------------
+// S = Q K^T: 16 columns of d per instruction, 4 instructions per 64-column
+// swizzled slab.  q_desc and k_desc describe the first slab of each tile;
+// every other operand address is a constant offset from them.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint32_t q_addr, uint32_t k_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    // 16 columns of d per instruction; 4 steps per 64-column swizzled slab
     const uint32_t off = (kk / 4) * kSlabBytes + (kk % 4) * 32;
-    umma_ss(tmem_s, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), idesc,
-            kk > 0 ? 1u : 0u);
+    umma_ss(tmem_s, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
+// O += P V: V is [keys][d] with d contiguous, an MN-major B operand.  16 keys
+// per instruction = two 8-row swizzle groups (2048 bytes); the 64-column
+// slabs of d are 16 KB apart (the descriptor's leading byte offset).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_addr,
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc,
                                          bool accumulate) {
-  // V is [keys][d] with d contiguous: an MN-major B operand.  16 keys per
-  // instruction = two 8-row swizzle groups (2048 bytes); the two 64-column
-  // slabs of d = 128 are 16 KB apart (leading byte offset).
   constexpr uint32_t idesc = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
+  umma_ts(tmem_o, tmem_p, v_desc, idesc, accumulate ? 1u : 0u);
 #pragma unroll
-  for (int kk = 0; kk < kBlockN / 16; ++kk) {
-    umma_ts(tmem_o, tmem_p + kk * 8, sdesc_sw128(v_addr + kk * 2048, kSlabBytes, 1024), idesc,
-            (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 1; kk < kBlockN / 16; ++kk)
+    umma_ts(tmem_o, tmem_p + kk * 8, sdesc_advance(v_desc, kk * 2048), idesc, 1u);
 }
 
 template <int D, bool CAUSAL>
@@ -232,8 +232,15 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     ok = ok && wait_phase(sy.kv_full0 + 8 * slot, (c / C::kStages) & 1u, sy, p, kSiteMma);
     return slot;
   };
-  auto q_addr = [&](int t) { return sbase + C::kQOff + t * C::kTileBytes; };
-  auto kv_addr = [&](uint32_t slot) { return sbase + C::kKVOff + slot * C::kTileBytes; };
+  // Descriptors are built once; per tile and per instruction they only move by
+  // constant offsets (the tensor core consumes one N=128 instruction every 64
+  // cycles, faster than a descriptor can be assembled from scratch).
+  const uint64_t q_desc0 = sdesc_sw128(sbase + C::kQOff, 16, 1024);
+  const uint64_t k_desc0 = sdesc_sw128(sbase + C::kKVOff, 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(sbase + C::kKVOff, kSlabBytes, 1024);
+  auto q_desc = [&](int t) { return sdesc_advance(q_desc0, t * C::kTileBytes); };
+  auto k_desc = [&](uint32_t slot) { return sdesc_advance(k_desc0, slot * C::kTileBytes); };
+  auto v_desc = [&](uint32_t slot) { return sdesc_advance(v_desc0, slot * C::kTileBytes); };
   auto tm_s = [&](int t) { return tmem + t * 128; };
   auto tm_o = [&](int t) { return tmem + 256 + t * 128; };
 
@@ -247,7 +254,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     }
     if (!ok) return;
     tc_fence_after_sync();
-    issue_pv<D>(tm_o(t), tm_s(t), kv_addr(vslot), jv > 0);
+    issue_pv<D>(tm_o(t), tm_s(t), v_desc(vslot), jv > 0);
     umma_commit(sy.o_done[t]);
   };
 
@@ -268,7 +275,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
       tc_fence_after_sync();
       for (int t = 0; t < kQTiles; ++t) {
         if (n[t] == 0) continue;
-        issue_qk<D>(tm_s(t), q_addr(t), kv_addr(ks));
+        issue_qk<D>(tm_s(t), q_desc(t), k_desc(ks));
         umma_commit(sy.s_full[t]);
         if (n[t] == 1) umma_commit(sy.q_empty[t]);
       }
@@ -282,7 +289,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
       if (!ok) break;
       if (jv < n[0]) pv_step(0, jv, vs);
       if (ok && have_k && j < n[0]) {
-        issue_qk<D>(tm_s(0), q_addr(0), kv_addr(ks));
+        issue_qk<D>(tm_s(0), q_desc(0), k_desc(ks));
         umma_commit(sy.s_full[0]);
         if (j == n[0] - 1) umma_commit(sy.q_empty[0]);
       }
@@ -291,7 +298,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
       umma_commit(sy.kv_empty0 + 8 * vs);
       if (have_k) {
         if (j < n[1]) {
-          issue_qk<D>(tm_s(1), q_addr(1), kv_addr(ks));
+          issue_qk<D>(tm_s(1), q_desc(1), k_desc(ks));
           umma_commit(sy.s_full[1]);
           if (j == n[1] - 1) umma_commit(sy.q_empty[1]);
         }

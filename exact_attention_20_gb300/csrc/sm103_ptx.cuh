@@ -194,6 +194,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor for a tile `bytes` further on.  The start address sits
+// in the low 14 bits as (address >> 4) and every shared address is below
+// 256 KB, so the add cannot carry into the other fields.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32
 // accumulator: D format in bits 4-5 (1 = f32), A format in 7-9 and B format in
 // 10-12 (1 = bf16), B major-ness in bit 16 (0 = K-major, 1 = MN-major),
