@@ -18,9 +18,10 @@
 //   warps 0-3  softmax warpgroup for query tile 0 (one row per thread)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q tiles once per item, then K_j, V_j into a ring
-//   warp  9    MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j on
-//              the tensor core, accumulators in tensor memory; owns TMEM.
-//   warps 10-11 idle (they complete the third warpgroup, which setmaxnreg needs)
+//   warps 9-10 MMA issuers, one thread each, one per query tile, taking
+//              turns: S_t = Q_t K_j^T and O_t += P_t V_j on the tensor core,
+//              accumulators in tensor memory; warp 9 owns the TMEM allocation
+//   warp  11   idle (it completes the third warpgroup, which setmaxnreg needs)
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 at column 0, S_1 at 128,
 // O_0 at 256, O_1 at 384.  P_t (bf16, two per column) overwrites the first
 // 64 columns of S_t and is the A operand of the P.V product.  While one
@@ -66,8 +67,8 @@ struct Cfg {
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2]
-  //           o_done[2] o_free[2] drain[1]
-  static constexpr int kNumBars = 2 * 2 + 2 * kStages + 2 * 4 + 1;
+  //           o_done[2] o_free[2] drain[1] turn[2]
+  static constexpr int kNumBars = 2 * 2 + 2 * kStages + 2 * 4 + 1 + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;           // + alignment slack
 };
@@ -107,6 +108,7 @@ __device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
 
 struct Sync {
   uint32_t q_full[2], q_empty[2], s_full[2], p_ready[2], o_done[2], o_free[2], drain;
+  uint32_t turn[2];              // hand-over between the two MMA issuers
   uint32_t kv_full0, kv_empty0;  // arrays of kStages barriers, 8 bytes apart
   volatile int* abort_flag;
 };
@@ -219,95 +221,96 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
     umma_ts(tmem_o, tmem_p + kk * 8, sdesc_advance(v_desc, kk * 2048), idesc, 1u);
 }
 
+// MMA issue is split between two threads, one per query tile, that take
+// strict turns.  A tcgen05.mma returns to its issuer roughly when the tensor
+// core accepts the next instruction, so a single issuer would leave the tensor
+// core idle while it checks barriers between groups.  Here the thread whose
+// turn it is feeds its group (O_t += P_t V_{j-1}, then S_t = Q_t K_j^T) while
+// the other thread has already done its waits and only needs the hand-over.
+// The tensor core therefore sees the same order as one issuer would produce:
+// tile 0's group, tile 1's group, tile 0's next group, ...  Each tile's
+// instructions stay in one thread, in issue order, so P_t(j-1) is read before
+// S_t(j) overwrites the same tensor-memory columns.
 template <int D, bool CAUSAL>
-__device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy, const FwdParams& p) {
+__device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, const Sync& sy,
+                                        const FwdParams& p) {
   using C = Cfg<D>;
-  uint32_t q_uses[2] = {0, 0};
-  uint32_t kv_count = 0;
-  uint32_t pr_par[2] = {0, 0};
-  uint32_t of_par[2] = {1, 1};
-  bool ok = true;
-  auto kv_slot_ready = [&](uint32_t c) -> uint32_t {
-    const uint32_t slot = c % C::kStages;
-    ok = ok && wait_phase(sy.kv_full0 + 8 * slot, (c / C::kStages) & 1u, sy, p, kSiteMma);
-    return slot;
-  };
+  const uint32_t bar_q_full = t ? sy.q_full[1] : sy.q_full[0];
+  const uint32_t bar_q_empty = t ? sy.q_empty[1] : sy.q_empty[0];
+  const uint32_t bar_s_full = t ? sy.s_full[1] : sy.s_full[0];
+  const uint32_t bar_p_ready = t ? sy.p_ready[1] : sy.p_ready[0];
+  const uint32_t bar_o_done = t ? sy.o_done[1] : sy.o_done[0];
+  const uint32_t bar_o_free = t ? sy.o_free[1] : sy.o_free[0];
+  const uint32_t my_turn = t ? sy.turn[1] : sy.turn[0];
+  const uint32_t next_turn = t ? sy.turn[0] : sy.turn[1];
   // Descriptors are built once; per tile and per instruction they only move by
   // constant offsets (the tensor core consumes one N=128 instruction every 64
   // cycles, faster than a descriptor can be assembled from scratch).
-  const uint64_t q_desc0 = sdesc_sw128(sbase + C::kQOff, 16, 1024);
+  const uint64_t q_desc = sdesc_advance(sdesc_sw128(sbase + C::kQOff, 16, 1024), t * C::kTileBytes);
   const uint64_t k_desc0 = sdesc_sw128(sbase + C::kKVOff, 16, 1024);
   const uint64_t v_desc0 = sdesc_sw128(sbase + C::kKVOff, kSlabBytes, 1024);
-  auto q_desc = [&](int t) { return sdesc_advance(q_desc0, t * C::kTileBytes); };
-  auto k_desc = [&](uint32_t slot) { return sdesc_advance(k_desc0, slot * C::kTileBytes); };
-  auto v_desc = [&](uint32_t slot) { return sdesc_advance(v_desc0, slot * C::kTileBytes); };
-  auto tm_s = [&](int t) { return tmem + t * 128; };
-  auto tm_o = [&](int t) { return tmem + 256 + t * 128; };
-
-  // O_t += P_t V for the item's key tile jv (first tile overwrites O_t).
-  auto pv_step = [&](int t, int jv, uint32_t vslot) {
-    ok = ok && wait_phase(sy.p_ready[t], pr_par[t], sy, p, kSiteMma);
-    pr_par[t] ^= 1u;
-    if (jv == 0) {
-      ok = ok && wait_phase(sy.o_free[t], of_par[t], sy, p, kSiteMma);
-      of_par[t] ^= 1u;
-    }
-    if (!ok) return;
-    tc_fence_after_sync();
-    issue_pv<D>(tm_o(t), tm_s(t), v_desc(vslot), jv > 0);
-    umma_commit(sy.o_done[t]);
+  const uint32_t tm_s = tmem + t * 128;
+  const uint32_t tm_o = tmem + 256 + t * 128;
+  uint32_t q_uses = 0, kv_count = 0, pr_par = 0, of_par = 1, turn_par = 0;
+  bool ok = true;
+  auto full = [&](uint32_t c) { return sy.kv_full0 + 8 * (c % C::kStages); };
+  auto empty = [&](uint32_t c) { return sy.kv_empty0 + 8 * (c % C::kStages); };
+  auto wait_full = [&](uint32_t c) {
+    ok = ok && wait_phase(full(c), (c / C::kStages) & 1u, sy, p, kSiteMma);
   };
+  auto release_unused = [&](uint32_t c) {  // a K/V tile this query tile skips
+    wait_full(c);                          // its previous phase is then complete
+    if (ok) mbar_arrive(empty(c));
+  };
+  if (t == 1) mbar_arrive(sy.turn[0]);  // tile 0 takes the first turn
 
   for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
     int rb, bh;
     decode_item(item, p, rb, bh);
-    const int n[2] = {tiles_for<CAUSAL>(rb, 0, p), tiles_for<CAUSAL>(rb, 1, p)};
-    const int nkv = max(n[0], n[1]);
-    for (int t = 0; t < kQTiles; ++t) {
-      if (n[t] == 0) continue;
-      ok = ok && wait_phase(sy.q_full[t], q_uses[t] & 1u, sy, p, kSiteMma);
-      ++q_uses[t];
+    const int n = tiles_for<CAUSAL>(rb, t, p);
+    const int nkv = max(n, tiles_for<CAUSAL>(rb, 1 - t, p));
+    if (n > 0) {
+      ok = ok && wait_phase(bar_q_full, q_uses & 1u, sy, p, kSiteMma);
+      ++q_uses;
     }
-    // key tile 0: S_0 and S_1
-    {
-      const uint32_t ks = kv_slot_ready(kv_count);
+    // step s issues O_t += P_t(s-1) V_{s-1} (if s >= 1) and S_t(s) (if s < n)
+    for (int s = 0; s <= nkv && ok; ++s) {
+      const bool do_pv = s >= 1 && s - 1 < n;
+      const bool do_s = s < n;
+      const uint32_t cv = kv_count + 2 * (s - 1) + 1;  // V_{s-1}
+      const uint32_t ck = kv_count + 2 * s;            // K_s
+      if (do_pv) {
+        wait_full(cv);
+        ok = ok && wait_phase(bar_p_ready, pr_par, sy, p, kSiteMma);
+        pr_par ^= 1u;
+        if (s == 1) {
+          ok = ok && wait_phase(bar_o_free, of_par, sy, p, kSiteMma);
+          of_par ^= 1u;
+        }
+      }
+      if (do_s) wait_full(ck);
+      ok = ok && wait_phase(my_turn, turn_par, sy, p, kSiteMma);
+      turn_par ^= 1u;
       if (!ok) break;
       tc_fence_after_sync();
-      for (int t = 0; t < kQTiles; ++t) {
-        if (n[t] == 0) continue;
-        issue_qk<D>(tm_s(t), q_desc(t), k_desc(ks));
-        umma_commit(sy.s_full[t]);
-        if (n[t] == 1) umma_commit(sy.q_empty[t]);
+      if (do_pv) {
+        issue_pv<D>(tm_o, tm_s, sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes), s > 1);
+        umma_commit(bar_o_done);
+        umma_commit(empty(cv));
       }
-      umma_commit(sy.kv_empty0 + 8 * ks);
-    }
-    for (int j = 1; j <= nkv && ok; ++j) {
-      const int jv = j - 1;                                   // value tile of this step
-      const uint32_t vs = kv_slot_ready(kv_count + 2 * jv + 1);
-      const bool have_k = j < nkv;
-      const uint32_t ks = have_k ? kv_slot_ready(kv_count + 2 * j) : 0u;
-      if (!ok) break;
-      if (jv < n[0]) pv_step(0, jv, vs);
-      if (ok && have_k && j < n[0]) {
-        issue_qk<D>(tm_s(0), q_desc(0), k_desc(ks));
-        umma_commit(sy.s_full[0]);
-        if (j == n[0] - 1) umma_commit(sy.q_empty[0]);
+      if (do_s) {
+        issue_qk<D>(tm_s, q_desc, sdesc_advance(k_desc0, (ck % C::kStages) * C::kTileBytes));
+        umma_commit(bar_s_full);
+        if (s == n - 1) umma_commit(bar_q_empty);
+        umma_commit(empty(ck));
       }
-      if (ok && jv < n[1]) pv_step(1, jv, vs);
-      if (!ok) break;
-      umma_commit(sy.kv_empty0 + 8 * vs);
-      if (have_k) {
-        if (j < n[1]) {
-          issue_qk<D>(tm_s(1), q_desc(1), k_desc(ks));
-          umma_commit(sy.s_full[1]);
-          if (j == n[1] - 1) umma_commit(sy.q_empty[1]);
-        }
-        umma_commit(sy.kv_empty0 + 8 * ks);
-      }
+      mbar_arrive(next_turn);
+      if (!do_pv && s >= 1) release_unused(cv);
+      if (!do_s && s < nkv) release_unused(ck);
     }
     kv_count += 2 * nkv;
   }
-  // Every MMA issued so far must finish before tensor memory is released.
+  // Every MMA this thread issued must finish before tensor memory is released.
   umma_commit(sy.drain);
   mbar_wait_bounded(sy.drain, 0, p.wait_limit_ns);
 }
@@ -451,7 +454,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       }
       tmem_st_wait();
       tc_fence_before_sync();
-      mbar_arrive(bar_p_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p_ready);  // one arrival per warp
     }
     if (!ok) break;
 
@@ -485,7 +489,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     }
     if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     tc_fence_before_sync();
-    mbar_arrive(bar_o_free);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_o_free);  // one arrival per warp
   }
 }
 
@@ -524,6 +529,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int t = 0; t < 2; ++t) sy.o_free[t] = b + 8 * t;
     b += 16;
     sy.drain = b;
+    b += 8;
+    for (int t = 0; t < 2; ++t) sy.turn[t] = b + 8 * t;
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
@@ -533,15 +540,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(sy.q_full[t], 1);
       mbar_init(sy.q_empty[t], 1);
       mbar_init(sy.s_full[t], 1);
-      mbar_init(sy.p_ready[t], kBlockM);
+      mbar_init(sy.p_ready[t], kBlockM / 32);  // one arrival per softmax warp
       mbar_init(sy.o_done[t], 1);
-      mbar_init(sy.o_free[t], kBlockM);
+      mbar_init(sy.o_free[t], kBlockM / 32);
     }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(sy.kv_full0 + 8 * s, 1);
-      mbar_init(sy.kv_empty0 + 8 * s, 1);
+      mbar_init(sy.kv_empty0 + 8 * s, 2);  // released by both MMA issuers
     }
-    mbar_init(sy.drain, 1);
+    mbar_init(sy.drain, 2);  // one commit from each MMA issuer
+    mbar_init(sy.turn[0], 1);
+    mbar_init(sy.turn[1], 1);
     *sy.abort_flag = 0;
     fence_barrier_init();
   }
@@ -564,8 +573,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (warp == kLoadWarp) {
       if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) run_mma<D, CAUSAL>(sbase, tmem, sy, p);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      if (lane == 0) run_mma<D, CAUSAL>(warp - kMmaWarp, sbase, tmem, sy, p);
       __syncwarp();
     }
   } else {
