@@ -289,21 +289,46 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
         }
       }
       if (do_s) wait_full(ck);
+      // Every operand of the group is computed before the turn is taken, so
+      // that the turn holds only the MMA instructions themselves.
+      uint64_t dv[kBlockN / 16], dq[D / 16], dk[D / 16];
+      {
+        const uint64_t v0 = sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes);
+        const uint64_t k0 = sdesc_advance(k_desc0, (ck % C::kStages) * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) dv[kk] = sdesc_advance(v0, kk * 2048);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kSlabBytes + (kk % 4) * 32;
+          dq[kk] = sdesc_advance(q_desc, off);
+          dk[kk] = sdesc_advance(k0, off);
+        }
+      }
+      const uint32_t acc0 = s > 1 ? 1u : 0u;
       ok = ok && wait_phase(my_turn, turn_par, sy, p, kSiteMma);
       turn_par ^= 1u;
       if (!ok) break;
       tc_fence_after_sync();
       if (do_pv) {
-        issue_pv<D>(tm_o, tm_s, sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes), s > 1);
-        umma_commit(bar_o_done);
-        umma_commit(empty(cv));
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_ts(tm_o, tm_s + kk * 8, dv[kk], idesc_pv, kk > 0 ? 1u : acc0);
       }
       if (do_s) {
-        issue_qk<D>(tm_s, q_desc, sdesc_advance(k_desc0, (ck % C::kStages) * C::kTileBytes));
-        umma_commit(bar_s_full);
-        if (s == n - 1) umma_commit(bar_q_empty);
-        umma_commit(empty(ck));
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_ss(tm_s, dq[kk], dk[kk], idesc_qk, kk > 0 ? 1u : 0u);
       }
+      // The commits come after both products so that the two run back to
+      // back, and before the hand-over so that they cannot be queued behind
+      // the other tile's group.  O_t's completion is then signalled with S_t's,
+      // which is when the softmax first needs it.
+      if (do_s) umma_commit(bar_s_full);
+      if (do_pv) umma_commit(bar_o_done);
+      if (do_s && s == n - 1) umma_commit(bar_q_empty);
+      if (do_pv) umma_commit(empty(cv));
+      if (do_s) umma_commit(empty(ck));
       mbar_arrive(next_turn);
       if (!do_pv && s >= 1) release_unused(cv);
       if (!do_s && s < nkv) release_unused(ck);
