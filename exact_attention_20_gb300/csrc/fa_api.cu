@@ -2,9 +2,12 @@
 // persistent-grid launch, and the device status word of the bounded waits.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "fa_gb300.h"
 #include "fa_fwd_kernel.cuh"
@@ -24,9 +27,13 @@ struct DeviceInfo {
   int num_sms = 0;
   int* status = nullptr;
   bool attr_set[2][2] = {{false, false}, {false, false}};
+  // Workspace for the parts of split items, one per stream so that calls on
+  // different streams never share it.  Allocated on a stream's first call.
+  std::vector<std::pair<cudaStream_t, float*>> workspaces;
 };
 
 std::mutex g_mu;
+std::mutex g_plan_mu;    // guards the shared launch parameter block
 DeviceInfo g_dev[kMaxDevices];
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -75,6 +82,145 @@ DeviceInfo* device_info(int* dev_out) {
   return &di;
 }
 
+// Host copy of the kernel's work accounting (decode_item, tiles_for, item_steps).
+struct PlanShape {
+  int N, BH, nkt, nrb;
+  bool causal;
+};
+
+int host_tiles_for(const PlanShape& s, int rb, int t) {
+  const int r0 = rb * fa::kItemRows + t * fa::kBlockM;
+  if (r0 >= s.N) return 0;
+  return s.causal ? std::min(r0 / fa::kBlockN + 1, s.nkt) : s.nkt;
+}
+
+int host_item_steps(const PlanShape& s, int item) {
+  int rb, bh;
+  fa::decode_item_shape(item, s.BH, s.nrb, rb, bh);
+  return std::max(host_tiles_for(s, rb, 0), host_tiles_for(s, rb, 1));
+}
+
+// Splits the concatenated steps of all items into `grid` equal contiguous
+// ranges (one per CTA) and lists the items that end up in several parts.
+// With no more items than SMs, each CTA takes one whole item instead.
+// Returns false when a split would need more parts per item than the merge
+// takes; the caller then uses whole items.
+bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams& p,
+               fa::MergeParams& mp, int& grid) {
+  const int items = s.BH * s.nrb;
+  mp.num_split = 0;
+  int nslots = 0;
+  if (!allow_split || items <= num_ctas) return false;
+  grid = num_ctas;
+  std::vector<long long> start(items + 1, 0);
+  for (int i = 0; i < items; ++i) start[i + 1] = start[i] + host_item_steps(s, i);
+  const long long W = start[items];
+  auto locate = [&](long long g, int& item, int& step) {
+    item = static_cast<int>(std::upper_bound(start.begin(), start.end(), g) - start.begin()) - 1;
+    step = static_cast<int>(g - start[item]);
+  };
+  auto item_cost = [&](int item) { return host_item_steps(s, item); };
+  auto add_part = [&](int item, int slot) {
+    const int k = mp.num_split;
+    if (k > 0 && mp.item[k - 1] == item) {
+      mp.slot_list[mp.first[k - 1] + mp.count[k - 1]] = slot;
+      ++mp.count[k - 1];
+      return;
+    }
+    mp.item[k] = item;
+    mp.first[k] = k == 0 ? 0 : mp.first[k - 1] + mp.count[k - 1];
+    mp.count[k] = 1;
+    mp.slot_list[mp.first[k]] = slot;
+    ++mp.num_split;
+  };
+  for (int c = 0; c < grid; ++c) {
+    const long long g0 = W * c / grid, g1 = W * (c + 1) / grid;
+    fa::WorkRange& r = p.range[c];
+    fa::SlotPair& sp = p.slots[c];
+    sp = {-1, -1};
+    if (g1 <= g0) {
+      r = {0, 0, -1, 0};
+      continue;
+    }
+    int ib, sb, il, sl;
+    locate(g0, ib, sb);
+    locate(g1 - 1, il, sl);
+    r = {ib, sb, il, sl + 1};
+    const int end0 = il == ib ? sl + 1 : item_cost(ib);
+    if (sb > 0 || end0 < item_cost(ib)) {
+      sp.first = nslots++;
+      add_part(ib, sp.first);
+    }
+    if (il != ib && sl + 1 < item_cost(il)) {
+      sp.last = nslots++;
+      add_part(il, sp.last);
+    }
+  }
+  for (int k = 0; k < mp.num_split; ++k)
+    if (mp.count[k] > fa::kMaxPartsPerItem) return false;
+  return true;
+}
+
+// The launch plan: fills p.range / p.slots (and mp's merge lists when items
+// are split) and returns the attention kernel's grid.
+int plan_launch(const PlanShape& shape, int num_ctas, bool allow_split, fa::FwdParams& p,
+                fa::MergeParams& mp) {
+  int grid = 0;
+  if (make_plan(shape, num_ctas, allow_split, p, mp, grid)) return grid;
+  // whole items: each CTA a contiguous run of whole items
+  mp.num_split = 0;
+  const int items = shape.BH * shape.nrb;
+  grid = std::min(items, num_ctas);
+  const int per = (items + grid - 1) / grid;
+  for (int c = 0; c < grid; ++c) {
+    const int a = c * per, b = std::min(items, (c + 1) * per) - 1;
+    p.range[c] = a <= b ? fa::WorkRange{a, 0, b, host_item_steps(shape, b)} : fa::WorkRange{0, 0, -1, 0};
+    p.slots[c] = {-1, -1};
+  }
+  return grid;
+}
+
+int num_ctas_for(const DeviceInfo* di, int max_ctas) {
+  int n = std::min(di->num_sms, fa::kMaxCtas);
+  return max_ctas > 0 ? std::min(n, max_ctas) : n;
+}
+
+// Workspace layout: part O [slots][256][128] fp32, then part LSE [slots][256] fp32.
+size_t ws_slots(const DeviceInfo* di) { return 2 * static_cast<size_t>(std::min(di->num_sms, fa::kMaxCtas)); }
+size_t ws_bytes(const DeviceInfo* di) { return ws_slots(di) * fa::kItemRows * (128 + 1) * sizeof(float); }
+
+float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto& w : di->workspaces)
+    if (w.first == stream) return w.second;
+  float* ptr = nullptr;
+  if (cudaMalloc(&ptr, ws_bytes(di)) != cudaSuccess) return nullptr;
+  di->workspaces.emplace_back(stream, ptr);
+  return ptr;
+}
+
+// Launches the merge of split items with programmatic stream serialisation:
+// its blocks may be scheduled while the attention grid drains, and wait for
+// that grid on the device before reading the parts.
+template <int D>
+cudaError_t launch_merge(const fa::MergeParams& mp, cudaStream_t stream) {
+  int max_parts = 0;
+  for (int k = 0; k < mp.num_split; ++k) max_parts = std::max(max_parts, mp.count[k]);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(mp.num_split * fa::merge_blocks_per_item<D>());
+  cfg.blockDim = dim3(fa::kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_parts <= 2) return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 2>, mp);
+  if (max_parts <= 4) return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 4>, mp);
+  return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 8>, mp);
+}
+
 template <int D, bool CAUSAL>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
            float scale, cudaStream_t stream, DeviceInfo* di, unsigned long long wait_limit_ns,
@@ -96,7 +242,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
       set = true;
     }
   }
-  fa::FwdParams p;
+  // large (work plan, merge lists): kept off the stack; guarded by g_plan_mu
+  static fa::FwdParams p;
+  static fa::MergeParams mp;
+  std::lock_guard<std::mutex> plan_lock(g_plan_mu);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.status = di->status;
@@ -108,10 +257,29 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit_ns = wait_limit_ns;
   p.starve_kv = starve_kv;
-  int grid = p.num_items < di->num_sms ? p.num_items : di->num_sms;
-  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
+  const PlanShape shape{N, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
+  const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, mp);
+  if (mp.num_split > 0) {
+    float* ws = stream_workspace(di, stream);
+    if (ws == nullptr) return FA_ERR_LAUNCH;
+    p.part_o = ws;
+    p.part_lse = ws + ws_slots(di) * fa::kItemRows * 128;
+  }
   fa::fa_fwd_kernel<D, CAUSAL><<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (mp.num_split > 0) {
+    mp.o = p.o;
+    mp.lse = lse;
+    mp.part_o = p.part_o;
+    mp.part_lse = p.part_lse;
+    mp.N = N;
+    mp.BH = BH;
+    mp.n_row_blocks = p.n_row_blocks;
+    if (launch_merge<D>(mp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
 }
 
 int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -179,6 +347,26 @@ int fa_watchdog_selftest(const void* q, const void* k, const void* v, void* o, f
                     lim, /*starve_kv=*/1, /*max_ctas=*/1);
   if (rc != FA_OK) return rc;
   return fa_get_device_status(stream);
+}
+
+int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_split_items) {
+  if (num_ctas == nullptr || num_split_items == nullptr) return FA_ERR_NULL;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1))
+    return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (di == nullptr) return FA_ERR_LAUNCH;
+  if (!di->supported) return FA_ERR_DEVICE;
+  const int BH = B * H;
+  const int nkt = (N + fa::kBlockN - 1) / fa::kBlockN;
+  const int nrb = (N + fa::kItemRows - 1) / fa::kItemRows;
+  static fa::FwdParams p;
+  static fa::MergeParams mp;
+  std::lock_guard<std::mutex> plan_lock(g_plan_mu);
+  *num_ctas = plan_launch(PlanShape{N, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p, mp);
+  *num_split_items = mp.num_split;
+  return FA_OK;
 }
 
 int fa_version(void) { return kVersion; }

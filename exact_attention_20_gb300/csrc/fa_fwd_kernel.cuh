@@ -73,10 +73,35 @@ struct Cfg {
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;           // + alignment slack
 };
 
+// Work distribution.  The forward's work is a list of items (256 query rows
+// of one batch*head), each made of steps (one 128-key tile visited by both
+// query tiles).  Every CTA gets a contiguous range of the concatenated steps
+// of equal length, so all SMs finish together.  A range boundary may fall
+// inside an item: each side then covers part of the item's keys and writes a
+// normalised partial result (O over its keys, and that part's logsumexp) to a
+// workspace slot, and a second kernel merges the parts through their
+// logsumexps (the merge of partial states over key ranges that Flash-Decoding
+// uses, "FlashAttention and kernels.").
+constexpr int kMaxCtas = 256;
+
+struct WorkRange {
+  int item_begin;  // first item touched
+  int step_begin;  // first step within it
+  int item_last;   // last item touched (item_last < item_begin: empty range)
+  int step_end;    // one past the last step within item_last
+};
+
+struct SlotPair {
+  int first;  // workspace slot of the first chunk when it is a part of an item, else -1
+  int last;   // the same for the last chunk (when it differs from the first)
+};
+
 struct FwdParams {
   __nv_bfloat16* o;        // [BH][N][D]
   float* lse;              // [BH][N]
   int* status;             // device status word (0 = ok)
+  float* part_o;           // workspace: [slot][256][D] fp32, O of a part, normalised within it
+  float* part_lse;         // workspace: [slot][256] fp32, the part's natural-log logsumexp
   int N;
   int BH;
   int n_key_tiles;         // ceil(N / 128)
@@ -85,15 +110,35 @@ struct FwdParams {
   float qk_scale;          // scale * log2(e)
   unsigned long long wait_limit_ns;
   int starve_kv;           // watchdog self-test: the producer never delivers K/V
+  WorkRange range[kMaxCtas];
+  SlotPair slots[kMaxCtas];
 };
 
-// Work item -> (row block, batch*head).  Heads vary fastest; row blocks run
-// from the last to the first, so under the causal mask the longest items
-// start first ("How to profile and optimise kernels", Round 5: reversed
-// query-tile order, heads on the fast axis).
+// Work item -> (row block, batch*head).  Row blocks are taken in pairs (the
+// last and the first, then the second-last and the second, ...) and the two
+// blocks of a pair alternate item by item, heads varying slowest within the
+// pair.  Under the causal mask a late row block visits many key tiles and an
+// early one few, so any contiguous run of items mixes long and short ones and
+// every CTA's range holds about the same number of items.  (The pages order
+// the longest tiles first, "How to profile and optimise kernels", Round 5;
+// with ranges of equal work the mix matters more than the order.)
+__host__ __device__ __forceinline__ void decode_item_shape(int item, int BH, int nrb, int& rb,
+                                                           int& bh) {
+  const int npairs = nrb / 2;
+  const int paired = 2 * BH * npairs;
+  if (item < paired) {
+    const int pair = item / (2 * BH);
+    const int r = item % (2 * BH);
+    bh = r / 2;
+    rb = (r & 1) ? pair : nrb - 1 - pair;
+  } else {  // the middle row block of an odd count
+    rb = npairs;
+    bh = item - paired;
+  }
+}
+
 __device__ __forceinline__ void decode_item(int item, const FwdParams& p, int& rb, int& bh) {
-  bh = item % p.BH;
-  rb = p.n_row_blocks - 1 - item / p.BH;
+  decode_item_shape(item, p.BH, p.n_row_blocks, rb, bh);
 }
 
 // Number of key tiles query tile t of row block rb visits (0 if the tile
@@ -104,6 +149,36 @@ __device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
   if (r0 >= p.N) return 0;
   if (CAUSAL) return min(r0 / kBlockN + 1, p.n_key_tiles);
   return p.n_key_tiles;
+}
+
+// Steps of an item: the key tiles its longer query tile visits.
+template <bool CAUSAL>
+__device__ __forceinline__ int item_steps(int rb, const FwdParams& p) {
+  return max(tiles_for<CAUSAL>(rb, 0, p), tiles_for<CAUSAL>(rb, 1, p));
+}
+
+// One chunk of this CTA's range: key tiles [kb, ke) of one item.
+struct Chunk {
+  int rb, bh;
+  int kb, ke;
+  int slot;   // workspace slot when the chunk is only a part of its item, else -1
+};
+
+__device__ __forceinline__ int num_chunks(const WorkRange& wr) {
+  return wr.item_last >= wr.item_begin ? wr.item_last - wr.item_begin + 1 : 0;
+}
+
+__device__ __forceinline__ int chunk_item(int q, const WorkRange& wr) { return wr.item_begin + q; }
+
+__device__ __forceinline__ Chunk chunk_of(int item, int nkv, const WorkRange& wr,
+                                          const SlotPair& sp, const FwdParams& p) {
+  Chunk c;
+  decode_item(item, p, c.rb, c.bh);
+  c.kb = item == wr.item_begin ? wr.step_begin : 0;
+  c.ke = item == wr.item_last ? wr.step_end : nkv;
+  const bool part = c.kb > 0 || c.ke < nkv;
+  c.slot = !part ? -1 : (item == wr.item_begin ? sp.first : sp.last);
+  return c;
 }
 
 struct Sync {
@@ -145,14 +220,16 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
   const uint64_t pol_q = l2_policy_evict_first();
   const uint64_t pol_kv = l2_policy_evict_last();
   bool ok = true;
-  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+  const WorkRange wr = p.range[blockIdx.x];
+  const SlotPair sp = p.slots[blockIdx.x];
+  for (int q = 0, nq = num_chunks(wr); q < nq && ok; ++q) {
+    const int item = chunk_item(q, wr);
     int rb, bh;
     decode_item(item, p, rb, bh);
-    const int n0 = tiles_for<CAUSAL>(rb, 0, p);
-    const int n1 = tiles_for<CAUSAL>(rb, 1, p);
-    const int nkv = max(n0, n1);
+    const int nkv = item_steps<CAUSAL>(rb, p);
+    const Chunk ch = chunk_of(item, nkv, wr, sp, p);
     for (int t = 0; t < kQTiles && ok; ++t) {
-      if ((t == 0 ? n0 : n1) == 0) continue;
+      if (min(ch.ke, tiles_for<CAUSAL>(rb, t, p)) <= ch.kb) continue;  // no tile of its own here
       ok = wait_phase(sy.q_empty[t], (q_loads[t] & 1u) ^ 1u, sy, p, kSiteProducer);
       if (!ok) break;
       ++q_loads[t];
@@ -164,7 +241,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
         tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * 64, row, bh, pol_q);
     }
     if (p.starve_kv) continue;  // self-test: never deliver K/V
-    for (int j = 0; j < nkv && ok; ++j) {
+    for (int j = ch.kb; j < ch.ke && ok; ++j) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t slot = kv_count % C::kStages;
@@ -264,26 +341,33 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
   };
   if (t == 1) mbar_arrive(sy.turn[0]);  // tile 0 takes the first turn
 
-  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
-    int rb, bh;
-    decode_item(item, p, rb, bh);
-    const int n = tiles_for<CAUSAL>(rb, t, p);
-    const int nkv = max(n, tiles_for<CAUSAL>(rb, 1 - t, p));
-    if (n > 0) {
+  const WorkRange wr = p.range[blockIdx.x];
+  const SlotPair sp = p.slots[blockIdx.x];
+  for (int q = 0, nq = num_chunks(wr); q < nq && ok; ++q) {
+    const int item = chunk_item(q, wr);
+    int rb0, bh0;
+    decode_item(item, p, rb0, bh0);
+    const int nkv_item = item_steps<CAUSAL>(rb0, p);
+    const Chunk ch = chunk_of(item, nkv_item, wr, sp, p);
+    // this query tile's key tiles inside the chunk: [kb, ne)
+    const int kb = ch.kb;
+    const int ne = min(ch.ke, tiles_for<CAUSAL>(ch.rb, t, p));
+    const int n_steps = ch.ke - kb;  // both issuers walk the same steps
+    if (ne > kb) {
       ok = ok && wait_phase(bar_q_full, q_uses & 1u, sy, p, kSiteMma);
       ++q_uses;
     }
-    // step s issues O_t += P_t(s-1) V_{s-1} (if s >= 1) and S_t(s) (if s < n)
-    for (int s = 0; s <= nkv && ok; ++s) {
-      const bool do_pv = s >= 1 && s - 1 < n;
-      const bool do_s = s < n;
-      const uint32_t cv = kv_count + 2 * (s - 1) + 1;  // V_{s-1}
-      const uint32_t ck = kv_count + 2 * s;            // K_s
+    // step s issues O_t += P_t(s-1) V_{s-1} (if kb <= s-1 < ne) and S_t(s) (if s < ne)
+    for (int s = kb; s <= ch.ke && ok; ++s) {
+      const bool do_pv = s - 1 >= kb && s - 1 < ne;
+      const bool do_s = s < ne;
+      const uint32_t cv = kv_count + 2 * (s - 1 - kb) + 1;  // V_{s-1}
+      const uint32_t ck = kv_count + 2 * (s - kb);          // K_s
       if (do_pv) {
         wait_full(cv);
         ok = ok && wait_phase(bar_p_ready, pr_par, sy, p, kSiteMma);
         pr_par ^= 1u;
-        if (s == 1) {
+        if (s == kb + 1) {
           ok = ok && wait_phase(bar_o_free, of_par, sy, p, kSiteMma);
           of_par ^= 1u;
         }
@@ -304,7 +388,7 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
           dk[kk] = sdesc_advance(k0, off);
         }
       }
-      const uint32_t acc0 = s > 1 ? 1u : 0u;
+      const uint32_t acc0 = s > kb + 1 ? 1u : 0u;
       ok = ok && wait_phase(my_turn, turn_par, sy, p, kSiteMma);
       turn_par ^= 1u;
       if (!ok) break;
@@ -326,18 +410,47 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       // which is when the softmax first needs it.
       if (do_s) umma_commit(bar_s_full);
       if (do_pv) umma_commit(bar_o_done);
-      if (do_s && s == n - 1) umma_commit(bar_q_empty);
+      if (do_s && s == ne - 1) umma_commit(bar_q_empty);
       if (do_pv) umma_commit(empty(cv));
       if (do_s) umma_commit(empty(ck));
       mbar_arrive(next_turn);
-      if (!do_pv && s >= 1) release_unused(cv);
-      if (!do_s && s < nkv) release_unused(ck);
+      if (!do_pv && s - 1 >= kb) release_unused(cv);
+      if (!do_s && s < ch.ke) release_unused(ck);
     }
-    kv_count += 2 * nkv;
+    kv_count += 2 * n_steps;
   }
   // Every MMA this thread issued must finish before tensor memory is released.
   umma_commit(sy.drain);
   mbar_wait_bounded(sy.drain, 0, p.wait_limit_ns);
+}
+
+// A warp publishes its 32 rows of one part of a split item: O normalised over
+// the part's keys (the accumulator scaled by inv_l) in fp32, and the part's
+// natural-log logsumexp.  An empty part (no key of the chunk lies at or below
+// the tile's rows) publishes L = -inf only; the merge gives it weight 0 and
+// never reads its O.
+template <int D>
+__device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_tile, uint32_t tO,
+                                             float inv_l, float lse_part, bool empty,
+                                             const FwdParams& p) {
+  const size_t prow = static_cast<size_t>(ch.slot) * kItemRows + t * kBlockM + row_in_tile;
+  if (!empty) {
+    float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+    const uint64_t il2 = f2_pack(inv_l, inv_l);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32_wait(tO + c * 32, o);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float a, b, e, f;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1])), il2), a, b);
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])), il2), e, f);
+        dst[c * 8 + i] = make_float4(a, b, e, f);
+      }
+    }
+  }
+  p.part_lse[prow] = lse_part;
 }
 
 // ---------------------------------------------------------------------------
@@ -362,12 +475,23 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   uint32_t s_par = 0, o_par = 0;
   bool ok = true;
 
-  for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
-    int rb, bh;
-    decode_item(item, p, rb, bh);
-    const int n = tiles_for<CAUSAL>(rb, t, p);
-    if (n == 0) continue;
+  const WorkRange wr = p.range[blockIdx.x];
+  const SlotPair sp = p.slots[blockIdx.x];
+  for (int q = 0, nq = num_chunks(wr); q < nq && ok; ++q) {
+    const int item = chunk_item(q, wr);
+    int rb0, bh0;
+    decode_item(item, p, rb0, bh0);
+    const Chunk ch = chunk_of(item, item_steps<CAUSAL>(rb0, p), wr, sp, p);
+    const int rb = ch.rb, bh = ch.bh;
+    const int n = tiles_for<CAUSAL>(rb, t, p);       // key tiles of this query tile in the item
+    const int ne = min(ch.ke, n);                    // ... and its part in this chunk: [kb, ne)
     const int row = rb * kItemRows + t * kBlockM + row_in_tile;
+    if (ne <= ch.kb) {
+      // No key tile of this query tile lies in the chunk (past its diagonal).
+      // A part still reports its rows, as an empty part: LSE = -inf.
+      if (ch.slot >= 0) publish_part<D>(ch, t, row_in_tile, tO, 0.f, -INFINITY, true, p);
+      continue;
+    }
     // m_ref: the reference maximum the exponentials are taken against (log2
     // units, already times qk_scale).  It is moved only when a tile's maximum
     // exceeds it by more than kRescaleThreshold, so P = exp2(s*qk - m_ref) may
@@ -378,7 +502,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     float l = 0.f;        // running sum of exp2(s*qk - m_ref), for the logsumexp
     float lq = 0.f;       // the same terms rounded to bf16 (what P.V multiplies), for O
 
-    for (int j = 0; j < n; ++j) {
+    for (int j = ch.kb; j < ne; ++j) {
       ok = wait_phase(bar_s_full, s_par, sy, p, kSiteSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -451,7 +575,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       l += sa + sb;
       lq += qa + qb;
 
-      if (j > 0) {
+      if (j > ch.kb) {
         // O_t holds the sum up to tile j-1; bring it to the new reference
         // maximum where a row moved it (alpha = 1 elsewhere, exact).
         ok = wait_phase(bar_o_done, o_par, sy, p, kSiteSoftmax);
@@ -492,27 +616,34 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     o_par ^= 1u;
     tc_fence_after_sync();
     const float inv_l = 1.f / lq;
-    const bool store = row < p.N;
-    __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+    const uint64_t il2 = f2_pack(inv_l, inv_l);
+    const float lse_row = (m_ref + log2f(l)) * 0.69314718055994531f;
+    if (ch.slot < 0) {
+      // the chunk is the whole item: final O in bf16 and LSE, rows < N only
+      const bool store = row < p.N;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32_wait(tO + c * 32, o);
-      uint32_t w[16];
-      const uint64_t il2 = f2_pack(inv_l, inv_l);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_wait(tO + c * 32, o);
+        uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float lo, hi;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2), lo, hi);
-        w[i] = pack_bf16x2(lo, hi);
+        for (int i = 0; i < 16; ++i) {
+          float lo, hi;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2), lo, hi);
+          w[i] = pack_bf16x2(lo, hi);
+        }
+        if (store) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
       }
-      if (store) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
+      if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = lse_row;
+    } else {
+      // a part of the item: merged with the other parts by fa_merge_kernel
+      publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_row, false, p);
     }
-    if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = (m_ref + log2f(l)) * 0.69314718055994531f;
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_o_free);  // one arrival per warp
@@ -592,6 +723,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();  // the merge of split items may be scheduled; it waits for this grid
 
   if (warp >= 8) {
     setmaxnreg_dec<kRegsAux>();
@@ -612,6 +744,115 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Merge of the parts of split items
+// ---------------------------------------------------------------------------
+// Each part r of a split item holds, per query row, O_r normalised over its
+// own keys and L_r, the natural log of its sum of exponentials.  The whole
+// row is L = ln sum_r exp(L_r) and O = sum_r exp(L_r - L) O_r (the combine of
+// partial softmax states over key ranges, Flash-Decoding, "FlashAttention and
+// kernels."), the largest L_r subtracted first; a part with L_r = -inf has no
+// key for the row, weight 0, and its O is not read.
+constexpr int kMaxPartsPerItem = 8;
+constexpr int kMergeThreads = 256;      // 8 warps
+
+struct MergeParams {
+  __nv_bfloat16* o;              // [BH][N][D]
+  float* lse;                    // [BH][N]
+  const float* part_o;           // workspace, as FwdParams::part_o
+  const float* part_lse;         // workspace, as FwdParams::part_lse
+  int N;
+  int BH;
+  int n_row_blocks;
+  int num_split;                 // split items
+  int item[kMaxCtas];            // the split items
+  int first[kMaxCtas];           // their first entry in slot_list
+  int count[kMaxCtas];           // their number of parts
+  int slot_list[2 * kMaxCtas];   // the parts' workspace slots, item after item
+};
+
+// Rows of one split item a merge warp takes: with d = 128 a row is one
+// float4 per lane; with d = 64 two rows share the warp.  Each warp handles
+// kMergeRowSets such row sets, every load issued before any is used.
+constexpr int kMergeRowSets = 2;
+
+template <int D>
+__host__ __device__ constexpr int merge_rows_per_block() {
+  return (kMergeThreads / 32) * (32 / (D / 4)) * kMergeRowSets;
+}
+
+// Blocks of fa_merge_kernel<D, P> per split item.
+template <int D>
+__host__ __device__ constexpr int merge_blocks_per_item() {
+  return kItemRows / merge_rows_per_block<D>();
+}
+
+// P bounds the parts of any split item of the launch (2, 4 or 8), so that
+// the per-part registers stay few and many blocks fit on an SM.  The parts
+// were written by the previous grid and do not change here: read-only loads.
+// A part with weight 0 is dropped by a select, so its O (never written, any
+// bit pattern) cannot reach the sum.
+template <int D, int P>
+__global__ void __launch_bounds__(kMergeThreads, P == 2 ? 8 : 1)
+fa_merge_kernel(const __grid_constant__ MergeParams mp) {
+  constexpr int kLanesPerRow = D / 4;
+  constexpr int kRowsPerSet = 32 / kLanesPerRow;
+  const int k = blockIdx.x / merge_blocks_per_item<D>();
+  const int sub = blockIdx.x % merge_blocks_per_item<D>();
+  int rb, bh;
+  decode_item_shape(mp.item[k], mp.BH, mp.n_row_blocks, rb, bh);
+  const int first = mp.first[k], count = mp.count[k];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col4 = lane % kLanesPerRow;
+  const int r0 = sub * merge_rows_per_block<D>() + warp * kRowsPerSet * kMergeRowSets + lane / kLanesPerRow;
+  size_t slot[P];
+#pragma unroll
+  for (int q = 0; q < P; ++q) slot[q] = q < count ? static_cast<size_t>(mp.slot_list[first + q]) : 0;
+  griddep_wait();  // the attention grid that wrote the parts has completed
+  float lr[kMergeRowSets][P];
+  float4 x[kMergeRowSets][P];
+#pragma unroll
+  for (int i = 0; i < kMergeRowSets; ++i) {
+    const int r = r0 + i * kRowsPerSet;
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      lr[i][q] = -INFINITY;
+      x[i][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < count && rb * kItemRows + r < mp.N) {
+        lr[i][q] = __ldg(mp.part_lse + slot[q] * kItemRows + r);
+        x[i][q] = __ldg(reinterpret_cast<const float4*>(mp.part_o + (slot[q] * kItemRows + r) * D) + col4);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kMergeRowSets; ++i) {
+    const int r = r0 + i * kRowsPerSet;
+    const int row = rb * kItemRows + r;
+    if (row >= mp.N) continue;
+    float m = lr[i][0];
+#pragma unroll
+    for (int q = 1; q < P; ++q) m = fmaxf(m, lr[i][q]);
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      const bool live = lr[i][q] != -INFINITY;
+      const float w = live ? exp2f((lr[i][q] - m) * 1.4426950408889634f) : 0.f;
+      wsum += w;
+      acc.x += live ? w * x[i][q].x : 0.f;
+      acc.y += live ? w * x[i][q].y : 0.f;
+      acc.z += live ? w * x[i][q].z : 0.f;
+      acc.w += live ? w * x[i][q].w : 0.f;
+    }
+    const float inv = 1.f / wsum;
+    uint2 out;
+    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(mp.o + (static_cast<size_t>(bh) * mp.N + row) * D)[col4] = out;
+    if (col4 == 0) mp.lse[static_cast<size_t>(bh) * mp.N + row] = m + logf(wsum);
   }
 }
 

@@ -30,6 +30,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _P, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
@@ -154,6 +155,25 @@ def attention_host(q, k, v, causal: bool = False, scale: float | None = None, de
         lseh.copy_(lsed, non_blocking=True)
     s.synchronize()
     return oh, lseh
+
+
+def plan(B: int, H: int, N: int, d: int, causal: bool = False) -> tuple[int, int]:
+    """(attention grid, split items) that fa_fwd uses for these sizes on the current device.
+
+    With split items > 0 a call makes two launches (attention, then the merge
+    of the parts), else one.
+    """
+    grid, nsplit = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().fa_fwd_plan(int(B), int(H), int(N), int(d), int(bool(causal)),
+                           ctypes.addressof(grid), ctypes.addressof(nsplit))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return grid.value, nsplit.value
+
+
+def launches_per_call(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
+    """Kernels one fa_fwd call launches for these sizes (1 or 2)."""
+    return 1 + (plan(B, H, N, d, causal)[1] > 0)
 
 
 def device_status(stream=None) -> int:

@@ -17,7 +17,13 @@
  *
  * Conventions shared by every entry point:
  *   - Pointers named q, k, v, o, lse are DEVICE pointers on the current device.
- *     The caller owns every buffer; nothing is allocated per call.
+ *     The caller owns every buffer it passes.  The library's own device
+ *     memory is a status word per device (static) and, per stream, one
+ *     workspace of 2 x (SMs, at most 256) x 256 x 129 fp32 values (about
+ *     40 MB on a GB300) for the parts of split work items, allocated on the
+ *     first fa_fwd on that stream that splits an item and kept until the
+ *     process exits.  Calls on one stream reuse its workspace in stream
+ *     order; calls on different streams never share one.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream) and return a status code.
  *   - Status 0 is FA_OK.  A negative status is returned for an error found
@@ -57,6 +63,15 @@ enum fa_status {
  *   scale   : multiplies Q.K before the softmax (typically 1/sqrt(d)); finite, > 0.
  *   stream  : cudaStream_t as void*.
  *
+ * Work division.  A work item is 256 query rows of one (b, h); its cost is
+ * the key tiles of 128 its longer half visits.  With more items than SMs,
+ * the concatenated steps of all items are cut into one equal contiguous
+ * range per SM; an item cut between two CTAs is computed in parts, each
+ * writing O normalised over its own keys and its logsumexp to the stream's
+ * workspace, and a second small kernel on the same stream merges the parts
+ * (O = sum_r exp(L_r - L) O_r, L = ln sum_r exp(L_r)).  Otherwise one CTA
+ * takes each item and there is one launch.  fa_fwd_plan reports the choice.
+ *
  * P (the softmax numerators) is rounded to bf16 before the P.V product and O
  * is rounded once to bf16 (round to nearest even) after the fp32 division by
  * the row sum ("How to profile and optimise kernels", the cast of P to bf16).
@@ -64,6 +79,17 @@ enum fa_status {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * fa_fwd_plan — the work division fa_fwd would use on the current device for
+ * these sizes (no pointer is needed and nothing is launched or allocated):
+ * *num_ctas = the attention kernel's grid, *num_split_items = items computed
+ * in parts (0: fa_fwd makes one launch; > 0: a merge launch follows).  The
+ * paper has no counterpart; it exists so that callers can size and count
+ * launches.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
+ * FA_ERR_INVALID_ARG (sizes as for fa_fwd), FA_ERR_DEVICE or FA_ERR_LAUNCH.
+ */
+int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_split_items);
 
 /* Human-readable name of a status code; never NULL, static storage. */
 const char* fa_strerror(int code);

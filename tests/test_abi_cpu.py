@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == ["fa_fwd", "fa_get_device_status", "fa_strerror", "fa_version",
-                     "fa_watchdog_selftest"]
+    assert names == ["fa_fwd", "fa_fwd_plan", "fa_get_device_status", "fa_strerror",
+                     "fa_version", "fa_watchdog_selftest"]
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -109,3 +109,21 @@ def test_binding_has_no_cpu_fallback(fa, monkeypatch):
     monkeypatch.setattr(fa, "LIB_PATH", "/nonexistent/libfa_gb300.so")
     with pytest.raises(RuntimeError):
         fa.lib()
+
+
+def test_plan_query_checks_its_arguments(fa):
+    import ctypes
+
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    pa, pb = ctypes.addressof(a), ctypes.addressof(b)
+    assert fa.lib().fa_fwd_plan(1, 32, 4096, 128, 0, None, pb) == fa.FA_ERR_NULL
+    assert fa.lib().fa_fwd_plan(1, 32, 4096, 128, 0, pa, None) == fa.FA_ERR_NULL
+    for args in ((0, 1, 128, 64, 0), (1, 1, 0, 64, 0), (1, 1, 128, 96, 0), (1, 1, 128, 64, 2),
+                 (1 << 12, 1 << 12, 1 << 12, 128, 0)):
+        assert fa.lib().fa_fwd_plan(*args, pa, pb) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="CPU-only check")
+def test_plan_query_without_a_device_fails_loudly(fa):
+    with pytest.raises(fa.FAError):
+        fa.plan(1, 32, 4096, 128, False)

@@ -123,10 +123,14 @@ def test_identical_keys_give_mean_of_visible_values(fa):
     assert d_o.max() <= 1e-2 and d_o.mean() <= 1e-3
 
 
-@pytest.mark.parametrize("N,d", [(129, 64), (1000, 128), (256, 128)])
+@pytest.mark.parametrize("B,H,N,d", [(2, 3, 129, 64), (2, 3, 1000, 128), (2, 3, 256, 128),
+                                     (4, 40, 1000, 64), (1, 33, 2304, 128), (1, 10, 4096, 64)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_guard_bands_untouched(fa, N, d, causal):
-    B, H, G = 2, 3, 4096
+def test_guard_bands_untouched(fa, B, H, N, d, causal):
+    # the last three shapes have more work items than SMs, so items are split
+    # across CTAs and merged; with 152 SMs, (1, 10, 4096) causal has ranges of
+    # about 18 steps against items of up to 32, so some items have three parts
+    G = 4096
     q, k, v = make_qkv(B, H, N, d, seed=9, device=DEV)
     n_o, n_l = B * H * N * d, B * H * N
     obuf = torch.full((n_o + 2 * G,), -512.0, dtype=torch.bfloat16, device=DEV)
@@ -188,3 +192,12 @@ def test_wrong_shapes_and_dtypes_raise(fa):
         fa.attention(q.transpose(2, 3), k, v)
     with pytest.raises(fa.FAError):
         fa.attention(make_qkv(1, 1, 16, 32, device=DEV)[0], *make_qkv(1, 1, 16, 32, device=DEV)[1:])
+
+
+def test_plan_reports_the_work_division(fa):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grid, nsplit = fa.plan(1, 32, 4096, 128, False)  # 512 items of 256 rows
+    assert grid == min(sms, 256) and 0 < nsplit <= grid
+    assert fa.launches_per_call(1, 32, 4096, 128, True) == 2
+    assert fa.plan(1, 2, 300, 64, True) == (4, 0)     # 4 items: one CTA each, one launch
+    assert fa.launches_per_call(1, 2, 300, 64, True) == 1
