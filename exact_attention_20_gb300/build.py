@@ -15,9 +15,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = [os.path.join(PKG, "csrc", "fa_api.cu")]
+SOURCES = [os.path.join(PKG, "csrc", n) for n in ("fa_api.cu", "fa_noalloc.cu")]
 DEPENDS = SOURCES + [
-    os.path.join(PKG, "csrc", n) for n in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh", "tma_host.h")
+    os.path.join(PKG, "csrc", n)
+    for n in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh", "tma_host.h", "fa_internal.h")
 ] + [os.path.join(ROOT, "include", "fa_gb300.h")]
 
 NVCC_FLAGS = [

@@ -11,6 +11,7 @@
 
 #include "fa_gb300.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_internal.h"
 #include "tma_host.h"
 
 namespace {
@@ -224,7 +225,7 @@ cudaError_t launch_merge(const fa::MergeParams& mp, cudaStream_t stream) {
 template <int D, bool CAUSAL>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
            float scale, cudaStream_t stream, DeviceInfo* di, unsigned long long wait_limit_ns,
-           int starve_kv, int max_ctas) {
+           int starve_kv, int max_ctas, const fa_internal::Scratch& fixed) {
   using C = fa::Cfg<D>;
   CUtensorMap tq, tk, tv;
   if (!fa::encode_bf16_3d(&tq, q, D, N, BH, 64, fa::kBlockM) ||
@@ -262,7 +263,10 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   const PlanShape shape{N, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
   const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, mp);
   if (mp.num_split > 0) {
-    float* ws = stream_workspace(di, stream);
+    // the caller's fixed scratch when given (checked to hold the workspace
+    // layout), else this stream's own workspace
+    if (fixed.ptr != nullptr && fixed.bytes < ws_bytes(di)) return FA_ERR_SCRATCH;
+    float* ws = fixed.ptr != nullptr ? fixed.ptr : stream_workspace(di, stream);
     if (ws == nullptr) return FA_ERR_LAUNCH;
     p.part_o = ws;
     p.part_lse = ws + ws_slots(di) * fa::kItemRows * 128;
@@ -284,7 +288,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, int causal, float scale, cudaStream_t stream, unsigned long long wait_limit_ns,
-             int starve_kv, int max_ctas) {
+             int starve_kv, int max_ctas, const fa_internal::Scratch& fixed) {
   int rc = check_args(q, k, v, o, lse, B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
   int dev = 0;
@@ -293,20 +297,35 @@ int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!di->supported) return FA_ERR_DEVICE;
   const int BH = B * H;
   if (d == 128)
-    return causal ? launch<128, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas)
-                  : launch<128, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas);
-  return causal ? launch<64, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas)
-                : launch<64, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas);
+    return causal ? launch<128, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
+                  : launch<128, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
+  return causal ? launch<64, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
+                : launch<64, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
 }
 
 }  // namespace
+
+namespace fa_internal {
+
+int check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   int B, int H, int N, int d, int causal, float scale) {
+  return check_args(q, k, v, o, lse, B, H, N, d, causal, scale);
+}
+
+int fwd_with_scratch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, int causal, float scale, void* stream, const Scratch& scratch) {
+  return dispatch(q, k, v, o, lse, B, H, N, d, causal, scale, static_cast<cudaStream_t>(stream),
+                  kWaitLimitNs, 0, 0, scratch);
+}
+
+}  // namespace fa_internal
 
 extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, int causal, float scale, void* stream) {
   return dispatch(q, k, v, o, lse, B, H, N, d, causal, scale, static_cast<cudaStream_t>(stream),
-                  kWaitLimitNs, 0, 0);
+                  kWaitLimitNs, 0, 0, fa_internal::Scratch{});
 }
 
 const char* fa_strerror(int code) {
@@ -319,6 +338,8 @@ const char* fa_strerror(int code) {
     case FA_ERR_DEVICE: return "FA_ERR_DEVICE: the current device is not sm_103 (GB300)";
     case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: a CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a pipeline wait inside the kernel gave up";
+    case FA_ERR_SCRATCH:
+      return "FA_ERR_SCRATCH: the work plan needs more scratch than fa_fwd_noalloc's static scratch holds";
     default: return "unknown fa status code";
   }
 }
@@ -344,7 +365,7 @@ int fa_watchdog_selftest(const void* q, const void* k, const void* v, void* o, f
   if (limit_ms < 1 || limit_ms > 10000) return FA_ERR_INVALID_ARG;
   const unsigned long long lim = static_cast<unsigned long long>(limit_ms) * 1000000ull;
   int rc = dispatch(q, k, v, o, lse, 1, 1, 128, 64, 0, 0.125f, static_cast<cudaStream_t>(stream),
-                    lim, /*starve_kv=*/1, /*max_ctas=*/1);
+                    lim, /*starve_kv=*/1, /*max_ctas=*/1, fa_internal::Scratch{});
   if (rc != FA_OK) return rc;
   return fa_get_device_status(stream);
 }

@@ -24,12 +24,14 @@ FA_ERR_ALIAS = -4
 FA_ERR_DEVICE = -5
 FA_ERR_LAUNCH = -6
 FA_ERR_DEVICE_TIMEOUT = -7
+FA_ERR_SCRATCH = -8
 
 # every function declared in include/fa_gb300.h, with its ctypes signature
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _P, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
@@ -99,6 +101,24 @@ def _check(name, t, dtype, shape, device):
 
 def fa_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None) -> None:
     """O and LSE into caller-owned tensors. q, k, v, o: bf16 [B, H, N, d]; lse: fp32 [B, H, N]."""
+    _call("fa_fwd", q, k, v, o, lse, causal, scale, stream)
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+                   stream=None) -> None:
+    """fa_fwd through the entry point that allocates no device memory at any call.
+
+    For callers that cannot let the library allocate once they run (a fixed
+    memory budget reserved at start-up, or no tolerance for an allocation
+    blocking on other streams).  The split-item parts go to one static
+    scratch per device, so calls that overlap on the GPU race on it; calls on
+    one stream are ordered.  The first call on a device does that device's
+    set-up and should come before any stream capture.
+    """
+    _call("fa_fwd_noalloc", q, k, v, o, lse, causal, scale, stream)
+
+
+def _call(entry, q, k, v, o, lse, causal, scale, stream) -> None:
     if q.dim() != 4:
         raise ValueError("q must be [B, H, N, d]")
     B, H, N, d = q.shape
@@ -111,8 +131,9 @@ def fa_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None, st
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(dev):
-        rc = lib().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                          B, H, N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+        rc = getattr(lib(), entry)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                   _stream_handle(stream))
     if rc != FA_OK:
         raise FAError(rc)
 

@@ -46,7 +46,8 @@ enum fa_status {
   FA_ERR_ALIAS = -4,          /* o or lse overlaps an input, or o overlaps lse */
   FA_ERR_DEVICE = -5,         /* current device is not compute capability 10.3 (sm_103a) */
   FA_ERR_LAUNCH = -6,         /* a CUDA call failed (tensor-map encoding, attribute, launch) */
-  FA_ERR_DEVICE_TIMEOUT = -7  /* a pipeline wait inside the kernel gave up (see fa_get_device_status) */
+  FA_ERR_DEVICE_TIMEOUT = -7, /* a pipeline wait inside the kernel gave up (see fa_get_device_status) */
+  FA_ERR_SCRATCH = -8         /* fa_fwd_noalloc: the device's work plan needs more than its static scratch */
 };
 
 /*
@@ -79,6 +80,39 @@ enum fa_status {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * fa_fwd_noalloc — fa_fwd (same arguments, kernels, work division and
+ * results) with no device allocation at any call: the parts of split items
+ * go to one static scratch array of FA_NOALLOC_SCRATCH_BYTES per device
+ * instead of the per-stream workspace.  The paper has no counterpart; it is
+ * for callers that must not allocate during a call, such as a server that
+ * reserves its whole memory budget at start-up, or one that cannot afford a
+ * cudaMalloc/cudaFree blocking on work queued on other streams.
+ *
+ *   - Limit: the scratch holds the workspace of up to FA_NOALLOC_MAX_CTAS
+ *     CTAs (two parts of 256 rows x 129 fp32 each per CTA); the work plan
+ *     uses one CTA per SM.  On a device with more SMs than that, a call
+ *     that splits items returns FA_ERR_SCRATCH and launches nothing.
+ *     Problem sizes are limited as for fa_fwd.
+ *   - Nothing in the scratch has to start at zero: every value the merge
+ *     reads is written earlier in the same call.
+ *   - The scratch is shared by every call on the device: calls whose work
+ *     overlaps on the GPU (e.g. on two streams at once) race on it and give
+ *     wrong results.  Calls on one stream are ordered and safe.
+ *   - The first call on a device does that device's set-up (device query,
+ *     the kernels' shared-memory attribute, the scratch's address); make
+ *     that first call before any stream capture.  The array lives in a
+ *     module of its own, loaded (and its device memory reserved by the CUDA
+ *     runtime) when the first call looks up its address, or when the
+ *     context is created if modules load eagerly.
+ * Returns FA_OK or a negative fa_status (the errors of fa_fwd, plus
+ * FA_ERR_SCRATCH).
+ */
+#define FA_NOALLOC_MAX_CTAS 160
+#define FA_NOALLOC_SCRATCH_BYTES (160u * 2u * 256u * 129u * 4u) /* 42,270,720 bytes */
+int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
  * fa_fwd_plan — the work division fa_fwd would use on the current device for

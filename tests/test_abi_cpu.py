@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == ["fa_fwd", "fa_fwd_plan", "fa_get_device_status", "fa_strerror",
-                     "fa_version", "fa_watchdog_selftest"]
+    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_get_device_status",
+                     "fa_strerror", "fa_version", "fa_watchdog_selftest"]
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 def test_version_and_strerror(fa):
     assert fa.version() == 100
-    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         msg = fa.strerror(code)
         assert msg.startswith("FA_")
     assert fa.strerror(12345) == "unknown fa status code"
@@ -127,3 +127,29 @@ def test_plan_query_checks_its_arguments(fa):
 def test_plan_query_without_a_device_fails_loudly(fa):
     with pytest.raises(fa.FAError):
         fa.plan(1, 32, 4096, 128, False)
+
+
+def test_noalloc_entry_checks_arguments_like_fa_fwd(fa):
+    # the host checks run before any CUDA call, with the same codes as fa_fwd
+    raw = fa.lib().fa_fwd_noalloc
+    assert raw(Q, K, V, O, L, 0, 1, 128, 64, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert raw(Q, K, V, O, L, 1, 1, 128, 96, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert raw(None, K, V, O, L, 1, 2, 256, 64, 0, 0.125, None) == fa.FA_ERR_NULL
+    assert raw(Q + 8, K, V, O, L, 1, 2, 256, 64, 0, 0.125, None) == fa.FA_ERR_ALIGN
+    assert raw(Q, K, V, Q, L, 1, 2, 256, 64, 0, 0.125, None) == fa.FA_ERR_ALIAS
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
+def test_noalloc_entry_without_a_device_fails_loudly(fa):
+    rc = fa.lib().fa_fwd_noalloc(Q, K, V, O, L, 1, 2, 256, 64, 0, 0.125, None)
+    assert rc in (fa.FA_ERR_LAUNCH, fa.FA_ERR_DEVICE)
+
+
+def test_noalloc_scratch_size_is_stated_in_the_header():
+    import re as _re
+
+    with open(HEADER) as f:
+        text = f.read()
+    ctas = int(_re.search(r"#define FA_NOALLOC_MAX_CTAS (\d+)", text).group(1))
+    assert ctas == 160
+    assert "42,270,720 bytes" in text and ctas * 2 * 256 * 129 * 4 == 42270720
