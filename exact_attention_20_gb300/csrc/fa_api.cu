@@ -31,6 +31,9 @@ struct DeviceInfo {
   // Workspace for the parts of split items, one per stream so that calls on
   // different streams never share it.  Allocated on a stream's first call.
   std::vector<std::pair<cudaStream_t, float*>> workspaces;
+  // Caller-supplied scratch areas used so far (their counters are cleared
+  // with the per-stream ones after a kernel gave up).
+  std::vector<float*> fixed_scratch;
 };
 
 std::mutex g_mu;
@@ -105,11 +108,11 @@ int host_item_steps(const PlanShape& s, int item) {
 // ranges (one per CTA) and lists the items that end up in several parts.
 // With no more items than SMs, each CTA takes one whole item instead.
 // Returns false when a split would need more parts per item than the merge
-// takes; the caller then uses whole items.
-bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams& p,
-               fa::MergeParams& mp, int& grid) {
+// takes; the caller then uses whole items.  num_split = split items.
+bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams& p, int& grid,
+               int& num_split) {
   const int items = s.BH * s.nrb;
-  mp.num_split = 0;
+  num_split = 0;
   int nslots = 0;
   if (!allow_split || items <= num_ctas) return false;
   grid = num_ctas;
@@ -121,24 +124,25 @@ bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams
     step = static_cast<int>(g - start[item]);
   };
   auto item_cost = [&](int item) { return host_item_steps(s, item); };
-  auto add_part = [&](int item, int slot) {
-    const int k = mp.num_split;
-    if (k > 0 && mp.item[k - 1] == item) {
-      mp.slot_list[mp.first[k - 1] + mp.count[k - 1]] = slot;
-      ++mp.count[k - 1];
-      return;
+  auto add_part = [&](int item, int slot) {  // returns the split item's index
+    const int k = num_split;
+    if (k > 0 && p.merge_item[k - 1] == item) {
+      p.merge_slots[p.merge_first[k - 1] + p.merge_count[k - 1]] = slot;
+      ++p.merge_count[k - 1];
+      return k - 1;
     }
-    mp.item[k] = item;
-    mp.first[k] = k == 0 ? 0 : mp.first[k - 1] + mp.count[k - 1];
-    mp.count[k] = 1;
-    mp.slot_list[mp.first[k]] = slot;
-    ++mp.num_split;
+    p.merge_item[k] = item;
+    p.merge_first[k] = k == 0 ? 0 : p.merge_first[k - 1] + p.merge_count[k - 1];
+    p.merge_count[k] = 1;
+    p.merge_slots[p.merge_first[k]] = slot;
+    ++num_split;
+    return k;
   };
   for (int c = 0; c < grid; ++c) {
     const long long g0 = W * c / grid, g1 = W * (c + 1) / grid;
     fa::WorkRange& r = p.range[c];
     fa::SlotPair& sp = p.slots[c];
-    sp = {-1, -1};
+    sp = {-1, -1, 0, 0};
     if (g1 <= g0) {
       r = {0, 0, -1, 0};
       continue;
@@ -150,33 +154,33 @@ bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams
     const int end0 = il == ib ? sl + 1 : item_cost(ib);
     if (sb > 0 || end0 < item_cost(ib)) {
       sp.first = nslots++;
-      add_part(ib, sp.first);
+      sp.k_first = add_part(ib, sp.first);
     }
     if (il != ib && sl + 1 < item_cost(il)) {
       sp.last = nslots++;
-      add_part(il, sp.last);
+      sp.k_last = add_part(il, sp.last);
     }
   }
-  for (int k = 0; k < mp.num_split; ++k)
-    if (mp.count[k] > fa::kMaxPartsPerItem) return false;
+  for (int k = 0; k < num_split; ++k)
+    if (p.merge_count[k] > fa::kMaxPartsPerItem) return false;
   return true;
 }
 
-// The launch plan: fills p.range / p.slots (and mp's merge lists when items
+// The launch plan: fills p.range / p.slots (and p's merge lists when items
 // are split) and returns the attention kernel's grid.
 int plan_launch(const PlanShape& shape, int num_ctas, bool allow_split, fa::FwdParams& p,
-                fa::MergeParams& mp) {
+                int& num_split) {
   int grid = 0;
-  if (make_plan(shape, num_ctas, allow_split, p, mp, grid)) return grid;
+  if (make_plan(shape, num_ctas, allow_split, p, grid, num_split)) return grid;
   // whole items: each CTA a contiguous run of whole items
-  mp.num_split = 0;
+  num_split = 0;
   const int items = shape.BH * shape.nrb;
   grid = std::min(items, num_ctas);
   const int per = (items + grid - 1) / grid;
   for (int c = 0; c < grid; ++c) {
     const int a = c * per, b = std::min(items, (c + 1) * per) - 1;
     p.range[c] = a <= b ? fa::WorkRange{a, 0, b, host_item_steps(shape, b)} : fa::WorkRange{0, 0, -1, 0};
-    p.slots[c] = {-1, -1};
+    p.slots[c] = {-1, -1, 0, 0};
   }
   return grid;
 }
@@ -186,9 +190,18 @@ int num_ctas_for(const DeviceInfo* di, int max_ctas) {
   return max_ctas > 0 ? std::min(n, max_ctas) : n;
 }
 
-// Workspace layout: part O [slots][256][128] fp32, then part LSE [slots][256] fp32.
+// Workspace layout: part O [slots][256][128] fp32, part LSE [slots][256]
+// fp32, then one arrival counter per split item (int, zero between launches).
 size_t ws_slots(const DeviceInfo* di) { return 2 * static_cast<size_t>(std::min(di->num_sms, fa::kMaxCtas)); }
-size_t ws_bytes(const DeviceInfo* di) { return ws_slots(di) * fa::kItemRows * (128 + 1) * sizeof(float); }
+size_t ws_counter_offset(const DeviceInfo* di) { return ws_slots(di) * fa::kItemRows * (128 + 1); }
+size_t ws_bytes(const DeviceInfo* di) { return (ws_counter_offset(di) + fa::kMaxCtas) * sizeof(float); }
+
+void remember_fixed_scratch(DeviceInfo* di, float* ws) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (float* f : di->fixed_scratch)
+    if (f == ws) return;
+  di->fixed_scratch.push_back(ws);
+}
 
 float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -196,30 +209,12 @@ float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
     if (w.first == stream) return w.second;
   float* ptr = nullptr;
   if (cudaMalloc(&ptr, ws_bytes(di)) != cudaSuccess) return nullptr;
+  if (cudaMemset(ptr + ws_counter_offset(di), 0, fa::kMaxCtas * sizeof(int)) != cudaSuccess) {
+    cudaFree(ptr);
+    return nullptr;
+  }
   di->workspaces.emplace_back(stream, ptr);
   return ptr;
-}
-
-// Launches the merge of split items with programmatic stream serialisation:
-// its blocks may be scheduled while the attention grid drains, and wait for
-// that grid on the device before reading the parts.
-template <int D>
-cudaError_t launch_merge(const fa::MergeParams& mp, cudaStream_t stream) {
-  int max_parts = 0;
-  for (int k = 0; k < mp.num_split; ++k) max_parts = std::max(max_parts, mp.count[k]);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(mp.num_split * fa::merge_blocks_per_item<D>());
-  cfg.blockDim = dim3(fa::kMergeThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (max_parts <= 2) return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 2>, mp);
-  if (max_parts <= 4) return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 4>, mp);
-  return cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<D, 8>, mp);
 }
 
 template <int D, bool CAUSAL>
@@ -245,7 +240,6 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   }
   // large (work plan, merge lists): kept off the stack; guarded by g_plan_mu
   static fa::FwdParams p;
-  static fa::MergeParams mp;
   std::lock_guard<std::mutex> plan_lock(g_plan_mu);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -261,28 +255,27 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.part_o = nullptr;
   p.part_lse = nullptr;
   const PlanShape shape{N, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
-  const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, mp);
-  if (mp.num_split > 0) {
+  int num_split = 0;
+  const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, num_split);
+  p.counters = nullptr;
+  if (num_split > 0) {
     // the caller's fixed scratch when given (checked to hold the workspace
-    // layout), else this stream's own workspace
-    if (fixed.ptr != nullptr && fixed.bytes < ws_bytes(di)) return FA_ERR_SCRATCH;
-    float* ws = fixed.ptr != nullptr ? fixed.ptr : stream_workspace(di, stream);
+    // layout; its counters start at zero), else this stream's own workspace
+    float* ws = nullptr;
+    if (fixed.ptr != nullptr) {
+      if (fixed.bytes < ws_bytes(di)) return FA_ERR_SCRATCH;
+      ws = fixed.ptr;
+      remember_fixed_scratch(di, ws);
+    } else {
+      ws = stream_workspace(di, stream);
+    }
     if (ws == nullptr) return FA_ERR_LAUNCH;
     p.part_o = ws;
     p.part_lse = ws + ws_slots(di) * fa::kItemRows * 128;
+    p.counters = reinterpret_cast<int*>(ws + ws_counter_offset(di));
   }
   fa::fa_fwd_kernel<D, CAUSAL><<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  if (mp.num_split > 0) {
-    mp.o = p.o;
-    mp.lse = lse;
-    mp.part_o = p.part_o;
-    mp.part_lse = p.part_lse;
-    mp.N = N;
-    mp.BH = BH;
-    mp.n_row_blocks = p.n_row_blocks;
-    if (launch_merge<D>(mp, stream) != cudaSuccess) return FA_ERR_LAUNCH;
-  }
   return FA_OK;
 }
 
@@ -357,6 +350,16 @@ int fa_get_device_status(void* stream) {
   const int zero = 0;
   if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return FA_ERR_LAUNCH;
+  // A kernel that gave up may have left arrival counters of split items
+  // non-zero: clear them in every workspace and scratch of this device.
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    std::vector<float*> areas = di->fixed_scratch;
+    for (auto& w : di->workspaces) areas.push_back(w.second);
+    for (float* a : areas)
+      if (cudaMemset(a + ws_counter_offset(di), 0, fa::kMaxCtas * sizeof(int)) != cudaSuccess)
+        return FA_ERR_LAUNCH;
+  }
   return FA_ERR_DEVICE_TIMEOUT;
 }
 
@@ -383,10 +386,11 @@ int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_
   const int nkt = (N + fa::kBlockN - 1) / fa::kBlockN;
   const int nrb = (N + fa::kItemRows - 1) / fa::kItemRows;
   static fa::FwdParams p;
-  static fa::MergeParams mp;
+  int num_split = 0;
   std::lock_guard<std::mutex> plan_lock(g_plan_mu);
-  *num_ctas = plan_launch(PlanShape{N, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p, mp);
-  *num_split_items = mp.num_split;
+  *num_ctas = plan_launch(PlanShape{N, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p,
+                          num_split);
+  *num_split_items = num_split;
   return FA_OK;
 }
 

@@ -79,9 +79,10 @@ struct Cfg {
 // of equal length, so all SMs finish together.  A range boundary may fall
 // inside an item: each side then covers part of the item's keys and writes a
 // normalised partial result (O over its keys, and that part's logsumexp) to a
-// workspace slot, and a second kernel merges the parts through their
-// logsumexps (the merge of partial states over key ranges that Flash-Decoding
-// uses, "FlashAttention and kernels.").
+// workspace slot.  The CTA whose arrival completes an item's parts merges
+// them through their logsumexps once its own work is done (the merge of
+// partial states over key ranges that Flash-Decoding uses, "FlashAttention
+// and kernels."); no CTA ever waits for another.
 constexpr int kMaxCtas = 256;
 
 struct WorkRange {
@@ -92,8 +93,10 @@ struct WorkRange {
 };
 
 struct SlotPair {
-  int first;  // workspace slot of the first chunk when it is a part of an item, else -1
-  int last;   // the same for the last chunk (when it differs from the first)
+  int first;    // workspace slot of the first chunk when it is a part of an item, else -1
+  int last;     // the same for the last chunk (when it differs from the first)
+  int k_first;  // the split item (index into the merge lists) of the first chunk
+  int k_last;   // ... and of the last chunk
 };
 
 struct FwdParams {
@@ -110,8 +113,13 @@ struct FwdParams {
   float qk_scale;          // scale * log2(e)
   unsigned long long wait_limit_ns;
   int starve_kv;           // watchdog self-test: the producer never delivers K/V
+  int* counters;           // workspace: per split item, softmax-warp arrivals (0 between launches)
   WorkRange range[kMaxCtas];
   SlotPair slots[kMaxCtas];
+  int merge_item[kMaxCtas];       // per split item: the item
+  int merge_first[kMaxCtas];      // ... its first entry in merge_slots
+  int merge_count[kMaxCtas];      // ... its number of parts
+  int merge_slots[2 * kMaxCtas];  // the parts' workspace slots, item after item
 };
 
 // Work item -> (row block, batch*head).  Row blocks are taken in pairs (the
@@ -162,6 +170,8 @@ struct Chunk {
   int rb, bh;
   int kb, ke;
   int slot;   // workspace slot when the chunk is only a part of its item, else -1
+  int k;      // its split item, when slot >= 0
+  int todo;   // 0 for the CTA's first chunk, 1 otherwise (its entry in Sync::merge_todo)
 };
 
 __device__ __forceinline__ int num_chunks(const WorkRange& wr) {
@@ -178,6 +188,8 @@ __device__ __forceinline__ Chunk chunk_of(int item, int nkv, const WorkRange& wr
   c.ke = item == wr.item_last ? wr.step_end : nkv;
   const bool part = c.kb > 0 || c.ke < nkv;
   c.slot = !part ? -1 : (item == wr.item_begin ? sp.first : sp.last);
+  c.k = item == wr.item_begin ? sp.k_first : sp.k_last;
+  c.todo = item == wr.item_begin ? 0 : 1;
   return c;
 }
 
@@ -186,6 +198,7 @@ struct Sync {
   uint32_t turn[2];              // hand-over between the two MMA issuers
   uint32_t kv_full0, kv_empty0;  // arrays of kStages barriers, 8 bytes apart
   volatile int* abort_flag;
+  volatile int* merge_todo;  // [2]: split items this CTA completed and merges at its end, else -1
 };
 
 // Bounded wait: true when the phase completed; false if this CTA is aborting
@@ -424,6 +437,8 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
   mbar_wait_bounded(sy.drain, 0, p.wait_limit_ns);
 }
 
+constexpr int kMaxPartsPerItem = 8;  // the plan splits no item into more parts
+
 // A warp publishes its 32 rows of one part of a split item: O normalised over
 // the part's keys (the accumulator scaled by inv_l) in fp32, and the part's
 // natural-log logsumexp.  An empty part (no key of the chunk lies at or below
@@ -451,6 +466,161 @@ __device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_
     }
   }
   p.part_lse[prow] = lse_part;
+}
+
+constexpr int kNumSoftmaxThreads = 2 * kBlockM;  // warps 0-7
+constexpr int kNumSoftmaxWarps = kNumSoftmaxThreads / 32;
+
+// A softmax warp has published its rows of one part: it counts its arrival on
+// the item's counter (after making its writes visible device-wide).  The warp
+// whose arrival completes every part of the item (parts x 8 warps) records
+// the item for this CTA to merge at its end.
+__device__ __forceinline__ void arrive_part(const Chunk& ch, int lane, const Sync& sy, const FwdParams& p) {
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) {
+    const int old = atomicAdd(p.counters + ch.k, 1);
+    if (old == p.merge_count[ch.k] * kNumSoftmaxWarps - 1) {
+      __threadfence();
+      sy.merge_todo[ch.todo] = ch.k;
+    }
+  }
+}
+
+// What the merge of one split item needs, copied out of the parameter block
+// so that the merge's stores cannot be taken to alias it.
+struct MergeArgs {
+  __nv_bfloat16* __restrict__ o;
+  float* __restrict__ lse;
+  const float* __restrict__ part_o;
+  const float* __restrict__ part_lse;
+  int N;
+  int rb, bh;
+  int count;
+  int slot[kMaxPartsPerItem];
+};
+
+// The 256 softmax threads merge one split item, every part of which is in
+// the workspace: L = ln sum_r exp(L_r), O = sum_r exp(L_r - L) O_r with the
+// largest L_r subtracted first, written as the final bf16 O and L.  Parts
+// with L_r = -inf weigh 0, and a select (not a product with 0) drops their O,
+// which was never written.
+//
+// Warp w takes rows 32w .. 32w+31 of the item.  Lane l first computes the
+// weights exp(L_r - L) and L of row 32w+l (one exponential per part and one
+// logarithm per row, LSE loads and stores coalesced); then, row after row,
+// the weights are broadcast and the lanes combine the row's O columns
+// (d = 128: lane l has columns 4l..4l+3; d = 64: two rows side by side),
+// with the loads of several rows in flight together.
+template <int D>
+__device__ __noinline__ void merge_item(const MergeArgs a) {
+  constexpr int kLanesPerRow = D / 4;
+  constexpr int kRowsPerPass = 32 / kLanesPerRow;  // rows combined side by side
+  constexpr int kPasses = 32 / kRowsPerPass;       // passes over the warp's 32 rows
+  constexpr int kBatch = 8;                        // passes whose loads are in flight together
+  static_assert(kNumSoftmaxWarps * 32 == kItemRows, "one warp per 32 rows");
+  static_assert(kPasses % kBatch == 0, "whole batches of passes");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col4 = lane % kLanesPerRow;
+  const int sub = lane / kLanesPerRow;
+  const int r0 = warp * 32;  // the warp's first row within the item
+  const int row0 = a.rb * kItemRows + r0;
+
+  // weights of row r0 + lane, normalised by their sum
+  float w[kMaxPartsPerItem];
+  {
+    float lr[kMaxPartsPerItem];
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) {
+      lr[q] = q < a.count ? __ldcg(a.part_lse + static_cast<size_t>(a.slot[q]) * kItemRows + r0 + lane)
+                          : -INFINITY;
+      m = fmaxf(m, lr[q]);
+    }
+    float wsum = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) {
+      w[q] = lr[q] == -INFINITY ? 0.f : exp2f((lr[q] - m) * 1.4426950408889634f);
+      wsum += w[q];
+    }
+    const float inv = 1.f / wsum;
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) w[q] *= inv;
+    if (row0 + lane < a.N) a.lse[static_cast<size_t>(a.bh) * a.N + row0 + lane] = m + logf(wsum);
+  }
+
+  const float4* src[kMaxPartsPerItem];
+#pragma unroll
+  for (int q = 0; q < kMaxPartsPerItem; ++q)
+    src[q] = reinterpret_cast<const float4*>(a.part_o + (static_cast<size_t>(a.slot[q]) * kItemRows + r0) * D);
+  uint2* dst = reinterpret_cast<uint2*>(a.o + (static_cast<size_t>(a.bh) * a.N + row0) * D);
+  auto combine = [&](const float4* x, const float* wr, int rr) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) {  // weight 0 past the item's parts
+      const bool live = wr[q] != 0.f;
+      acc.x += live ? wr[q] * x[q].x : 0.f;
+      acc.y += live ? wr[q] * x[q].y : 0.f;
+      acc.z += live ? wr[q] * x[q].z : 0.f;
+      acc.w += live ? wr[q] * x[q].w : 0.f;
+    }
+    if (row0 + rr < a.N)
+      dst[rr * (D / 4) + col4] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  };
+  if (a.count == 2) {
+    for (int b = 0; b < kPasses; b += kBatch) {
+      float4 x[kBatch][2];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int rr = (b + i) * kRowsPerPass + sub;
+        x[i][0] = __ldcg(src[0] + rr * (D / 4) + col4);
+        x[i][1] = __ldcg(src[1] + rr * (D / 4) + col4);
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int rr = (b + i) * kRowsPerPass + sub;
+        const float wr[2] = {__shfl_sync(0xffffffffu, w[0], rr), __shfl_sync(0xffffffffu, w[1], rr)};
+        float4 acc;
+        acc.x = (wr[0] != 0.f ? wr[0] * x[i][0].x : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].x : 0.f);
+        acc.y = (wr[0] != 0.f ? wr[0] * x[i][0].y : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].y : 0.f);
+        acc.z = (wr[0] != 0.f ? wr[0] * x[i][0].z : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].z : 0.f);
+        acc.w = (wr[0] != 0.f ? wr[0] * x[i][0].w : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].w : 0.f);
+        if (row0 + rr < a.N)
+          dst[rr * (D / 4) + col4] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      }
+    }
+  } else {
+    for (int pass = 0; pass < kPasses; ++pass) {
+      const int rr = pass * kRowsPerPass + sub;
+      float4 x[kMaxPartsPerItem];
+      float wr[kMaxPartsPerItem];
+#pragma unroll
+      for (int q = 0; q < kMaxPartsPerItem; ++q) {
+        x[q] = q < a.count ? __ldcg(src[q] + rr * (D / 4) + col4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wr[q] = __shfl_sync(0xffffffffu, w[q], rr);
+      }
+      combine(x, wr, rr);
+    }
+  }
+}
+
+// Merges split item k (called by the 256 softmax threads) and resets its
+// counter for the next launch: every arrival for the item has happened.
+template <int D>
+__device__ __forceinline__ void merge_split_item(int k, const FwdParams& p) {
+  MergeArgs a;
+  a.o = p.o;
+  a.lse = p.lse;
+  a.part_o = p.part_o;
+  a.part_lse = p.part_lse;
+  a.N = p.N;
+  decode_item(p.merge_item[k], p, a.rb, a.bh);
+  a.count = p.merge_count[k];
+  const int first = p.merge_first[k];
+#pragma unroll
+  for (int q = 0; q < kMaxPartsPerItem; ++q) a.slot[q] = q < a.count ? p.merge_slots[first + q] : 0;
+  if (threadIdx.x == 0) p.counters[k] = 0;
+  merge_item<D>(a);
 }
 
 // ---------------------------------------------------------------------------
@@ -489,7 +659,10 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     if (ne <= ch.kb) {
       // No key tile of this query tile lies in the chunk (past its diagonal).
       // A part still reports its rows, as an empty part: LSE = -inf.
-      if (ch.slot >= 0) publish_part<D>(ch, t, row_in_tile, tO, 0.f, -INFINITY, true, p);
+      if (ch.slot >= 0) {
+        publish_part<D>(ch, t, row_in_tile, tO, 0.f, -INFINITY, true, p);
+        arrive_part(ch, lane, sy, p);
+      }
       continue;
     }
     // m_ref: the reference maximum the exponentials are taken against (log2
@@ -641,8 +814,9 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       }
       if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = lse_row;
     } else {
-      // a part of the item: merged with the other parts by fa_merge_kernel
+      // a part of the item: merged once every part is in (merge_item)
       publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_row, false, p);
+      arrive_part(ch, lane, sy, p);
     }
     tc_fence_before_sync();
     __syncwarp();
@@ -690,6 +864,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  sy.merge_todo = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -708,6 +883,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(sy.turn[0], 1);
     mbar_init(sy.turn[1], 1);
     *sy.abort_flag = 0;
+    sy.merge_todo[0] = -1;
+    sy.merge_todo[1] = -1;
     fence_barrier_init();
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -723,7 +900,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  griddep_launch_dependents();  // the merge of split items may be scheduled; it waits for this grid
 
   if (warp >= 8) {
     setmaxnreg_dec<kRegsAux>();
@@ -737,6 +913,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
     run_softmax<D, CAUSAL>(warp >> 2, tmem, sy, p);
+    // The softmax warps merge the split items this CTA completed, after all
+    // their own work (merge_todo is final once all eight have passed here).
+    named_bar_sync(1, kNumSoftmaxThreads);
+    if (*sy.abort_flag == 0) {
+      for (int i = 0; i < 2; ++i) {
+        const int k = sy.merge_todo[i];
+        if (k >= 0) merge_split_item<D>(k, p);
+      }
+    }
   }
 
   tc_fence_before_sync();
@@ -744,115 +929,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Merge of the parts of split items
-// ---------------------------------------------------------------------------
-// Each part r of a split item holds, per query row, O_r normalised over its
-// own keys and L_r, the natural log of its sum of exponentials.  The whole
-// row is L = ln sum_r exp(L_r) and O = sum_r exp(L_r - L) O_r (the combine of
-// partial softmax states over key ranges, Flash-Decoding, "FlashAttention and
-// kernels."), the largest L_r subtracted first; a part with L_r = -inf has no
-// key for the row, weight 0, and its O is not read.
-constexpr int kMaxPartsPerItem = 8;
-constexpr int kMergeThreads = 256;      // 8 warps
-
-struct MergeParams {
-  __nv_bfloat16* o;              // [BH][N][D]
-  float* lse;                    // [BH][N]
-  const float* part_o;           // workspace, as FwdParams::part_o
-  const float* part_lse;         // workspace, as FwdParams::part_lse
-  int N;
-  int BH;
-  int n_row_blocks;
-  int num_split;                 // split items
-  int item[kMaxCtas];            // the split items
-  int first[kMaxCtas];           // their first entry in slot_list
-  int count[kMaxCtas];           // their number of parts
-  int slot_list[2 * kMaxCtas];   // the parts' workspace slots, item after item
-};
-
-// Rows of one split item a merge warp takes: with d = 128 a row is one
-// float4 per lane; with d = 64 two rows share the warp.  Each warp handles
-// kMergeRowSets such row sets, every load issued before any is used.
-constexpr int kMergeRowSets = 2;
-
-template <int D>
-__host__ __device__ constexpr int merge_rows_per_block() {
-  return (kMergeThreads / 32) * (32 / (D / 4)) * kMergeRowSets;
-}
-
-// Blocks of fa_merge_kernel<D, P> per split item.
-template <int D>
-__host__ __device__ constexpr int merge_blocks_per_item() {
-  return kItemRows / merge_rows_per_block<D>();
-}
-
-// P bounds the parts of any split item of the launch (2, 4 or 8), so that
-// the per-part registers stay few and many blocks fit on an SM.  The parts
-// were written by the previous grid and do not change here: read-only loads.
-// A part with weight 0 is dropped by a select, so its O (never written, any
-// bit pattern) cannot reach the sum.
-template <int D, int P>
-__global__ void __launch_bounds__(kMergeThreads, P == 2 ? 8 : 1)
-fa_merge_kernel(const __grid_constant__ MergeParams mp) {
-  constexpr int kLanesPerRow = D / 4;
-  constexpr int kRowsPerSet = 32 / kLanesPerRow;
-  const int k = blockIdx.x / merge_blocks_per_item<D>();
-  const int sub = blockIdx.x % merge_blocks_per_item<D>();
-  int rb, bh;
-  decode_item_shape(mp.item[k], mp.BH, mp.n_row_blocks, rb, bh);
-  const int first = mp.first[k], count = mp.count[k];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col4 = lane % kLanesPerRow;
-  const int r0 = sub * merge_rows_per_block<D>() + warp * kRowsPerSet * kMergeRowSets + lane / kLanesPerRow;
-  size_t slot[P];
-#pragma unroll
-  for (int q = 0; q < P; ++q) slot[q] = q < count ? static_cast<size_t>(mp.slot_list[first + q]) : 0;
-  griddep_wait();  // the attention grid that wrote the parts has completed
-  float lr[kMergeRowSets][P];
-  float4 x[kMergeRowSets][P];
-#pragma unroll
-  for (int i = 0; i < kMergeRowSets; ++i) {
-    const int r = r0 + i * kRowsPerSet;
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-      lr[i][q] = -INFINITY;
-      x[i][q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (q < count && rb * kItemRows + r < mp.N) {
-        lr[i][q] = __ldg(mp.part_lse + slot[q] * kItemRows + r);
-        x[i][q] = __ldg(reinterpret_cast<const float4*>(mp.part_o + (slot[q] * kItemRows + r) * D) + col4);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < kMergeRowSets; ++i) {
-    const int r = r0 + i * kRowsPerSet;
-    const int row = rb * kItemRows + r;
-    if (row >= mp.N) continue;
-    float m = lr[i][0];
-#pragma unroll
-    for (int q = 1; q < P; ++q) m = fmaxf(m, lr[i][q]);
-    float wsum = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < P; ++q) {
-      const bool live = lr[i][q] != -INFINITY;
-      const float w = live ? exp2f((lr[i][q] - m) * 1.4426950408889634f) : 0.f;
-      wsum += w;
-      acc.x += live ? w * x[i][q].x : 0.f;
-      acc.y += live ? w * x[i][q].y : 0.f;
-      acc.z += live ? w * x[i][q].z : 0.f;
-      acc.w += live ? w * x[i][q].w : 0.f;
-    }
-    const float inv = 1.f / wsum;
-    uint2 out;
-    out.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-    out.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(mp.o + (static_cast<size_t>(bh) * mp.N + row) * D)[col4] = out;
-    if (col4 == 0) mp.lse[static_cast<size_t>(bh) * mp.N + row] = m + logf(wsum);
   }
 }
 

@@ -19,8 +19,9 @@
 namespace {
 
 // Room for the split-item workspace of up to 160 CTAs at d <= 128:
-// 2 parts per CTA x 256 rows x (128 O values + 1 logsumexp) fp32.
-constexpr size_t kScratchFloats = static_cast<size_t>(FA_NOALLOC_MAX_CTAS) * 2 * 256 * 129;
+// 2 parts per CTA x 256 rows x (128 O values + 1 logsumexp) fp32, then 256
+// arrival counters (one per split item).
+constexpr size_t kScratchFloats = static_cast<size_t>(FA_NOALLOC_MAX_CTAS) * 2 * 256 * 129 + 256;
 static_assert(kScratchFloats * sizeof(float) == FA_NOALLOC_SCRATCH_BYTES,
               "the header states the scratch size");
 
@@ -31,12 +32,16 @@ std::mutex g_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
 
 // The scratch's device address on the current device, looked up once per
-// device (with that device current); nullptr if the lookup failed.
+// device (with that device current); nullptr if the set-up failed.  The
+// set-up also clears the whole array, so that the arrival counters start at
+// zero (every call leaves them at zero again).
 float* scratch_address(int dev) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) return nullptr;
+    if (cudaMemset(p, 0, kScratchFloats * sizeof(float)) != cudaSuccess) return nullptr;
+    if (cudaDeviceSynchronize() != cudaSuccess) return nullptr;
     g_scratch_ptr[dev] = static_cast<float*>(p);
   }
   return g_scratch_ptr[dev];

@@ -181,8 +181,7 @@ def attention_host(q, k, v, causal: bool = False, scale: float | None = None, de
 def plan(B: int, H: int, N: int, d: int, causal: bool = False) -> tuple[int, int]:
     """(attention grid, split items) that fa_fwd uses for these sizes on the current device.
 
-    With split items > 0 a call makes two launches (attention, then the merge
-    of the parts), else one.
+    Split items are computed in parts and merged inside the same launch.
     """
     grid, nsplit = ctypes.c_int(0), ctypes.c_int(0)
     rc = lib().fa_fwd_plan(int(B), int(H), int(N), int(d), int(bool(causal)),
@@ -192,9 +191,7 @@ def plan(B: int, H: int, N: int, d: int, causal: bool = False) -> tuple[int, int
     return grid.value, nsplit.value
 
 
-def launches_per_call(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
-    """Kernels one fa_fwd call launches for these sizes (1 or 2)."""
-    return 1 + (plan(B, H, N, d, causal)[1] > 0)
+KERNELS_PER_CALL = 1  # every fa_fwd call is one kernel launch
 
 
 def device_status(stream=None) -> int:

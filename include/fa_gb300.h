@@ -20,7 +20,8 @@
  *     The caller owns every buffer it passes.  The library's own device
  *     memory is a status word per device (static) and, per stream, one
  *     workspace of 2 x (SMs, at most 256) x 256 x 129 fp32 values (about
- *     40 MB on a GB300) for the parts of split work items, allocated on the
+ *     40 MB on a GB300) plus 256 counters for the parts of split work
+ *     items, allocated (and its counters zeroed) on the
  *     first fa_fwd on that stream that splits an item and kept until the
  *     process exits.  Calls on one stream reuse its workspace in stream
  *     order; calls on different streams never share one.
@@ -69,9 +70,10 @@ enum fa_status {
  * the concatenated steps of all items are cut into one equal contiguous
  * range per SM; an item cut between two CTAs is computed in parts, each
  * writing O normalised over its own keys and its logsumexp to the stream's
- * workspace, and a second small kernel on the same stream merges the parts
- * (O = sum_r exp(L_r - L) O_r, L = ln sum_r exp(L_r)).  Otherwise one CTA
- * takes each item and there is one launch.  fa_fwd_plan reports the choice.
+ * workspace; the CTA whose arrival completes an item's parts merges them
+ * (O = sum_r exp(L_r - L) O_r, L = ln sum_r exp(L_r)) after its own work, so
+ * a call is always one launch.  Otherwise one CTA takes each item.
+ * fa_fwd_plan reports the choice.
  *
  * P (the softmax numerators) is rounded to bf16 before the P.V product and O
  * is rounded once to bf16 (round to nearest even) after the fp32 division by
@@ -91,12 +93,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * cudaMalloc/cudaFree blocking on work queued on other streams.
  *
  *   - Limit: the scratch holds the workspace of up to FA_NOALLOC_MAX_CTAS
- *     CTAs (two parts of 256 rows x 129 fp32 each per CTA); the work plan
+ *     CTAs (two parts of 256 rows x 129 fp32 each per CTA, and one arrival
+ *     counter per split item); the work plan
  *     uses one CTA per SM.  On a device with more SMs than that, a call
  *     that splits items returns FA_ERR_SCRATCH and launches nothing.
  *     Problem sizes are limited as for fa_fwd.
- *   - Nothing in the scratch has to start at zero: every value the merge
- *     reads is written earlier in the same call.
+ *   - The arrival counters must start at zero: the first call's set-up
+ *     clears the scratch, and every call leaves the counters at zero again.
+ *     A call whose kernel gave up on a wait (FA_ERR_DEVICE_TIMEOUT) may
+ *     leave them non-zero; fa_get_device_status, which reports that, clears
+ *     them.  Nothing else has to start at any value.
  *   - The scratch is shared by every call on the device: calls whose work
  *     overlaps on the GPU (e.g. on two streams at once) race on it and give
  *     wrong results.  Calls on one stream are ordered and safe.
@@ -110,7 +116,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * FA_ERR_SCRATCH).
  */
 #define FA_NOALLOC_MAX_CTAS 160
-#define FA_NOALLOC_SCRATCH_BYTES (160u * 2u * 256u * 129u * 4u) /* 42,270,720 bytes */
+#define FA_NOALLOC_SCRATCH_BYTES ((160u * 2u * 256u * 129u + 256u) * 4u) /* 42,271,744 bytes */
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int N, int d, int causal, float scale, void* stream);
 
@@ -118,9 +124,8 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  * fa_fwd_plan — the work division fa_fwd would use on the current device for
  * these sizes (no pointer is needed and nothing is launched or allocated):
  * *num_ctas = the attention kernel's grid, *num_split_items = items computed
- * in parts (0: fa_fwd makes one launch; > 0: a merge launch follows).  The
- * paper has no counterpart; it exists so that callers can size and count
- * launches.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
+ * in parts (merged inside the same launch).  The paper has no counterpart;
+ * it exists so that callers can see how the work is divided.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
  * FA_ERR_INVALID_ARG (sizes as for fa_fwd), FA_ERR_DEVICE or FA_ERR_LAUNCH.
  */
 int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_split_items);

@@ -198,6 +198,4 @@ def test_plan_reports_the_work_division(fa):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     grid, nsplit = fa.plan(1, 32, 4096, 128, False)  # 512 items of 256 rows
     assert grid == min(sms, 256) and 0 < nsplit <= grid
-    assert fa.launches_per_call(1, 32, 4096, 128, True) == 2
-    assert fa.plan(1, 2, 300, 64, True) == (4, 0)     # 4 items: one CTA each, one launch
-    assert fa.launches_per_call(1, 2, 300, 64, True) == 1
+    assert fa.plan(1, 2, 300, 64, True) == (4, 0)     # 4 items: one CTA each
