@@ -345,14 +345,20 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
   bool ok = true;
   auto full = [&](uint32_t c) { return sy.kv_full0 + 8 * (c % C::kStages); };
   auto empty = [&](uint32_t c) { return sy.kv_empty0 + 8 * (c % C::kStages); };
-  auto wait_full = [&](uint32_t c) {
-    ok = ok && wait_phase(full(c), (c / C::kStages) & 1u, sy, p, kSiteMma);
+  // The whole warp runs this loop, so that everything but the MMA
+  // instructions themselves is warp-uniform (descriptors live in uniform
+  // registers); every wait is voted so the warp stays converged, and one
+  // lane issues the MMAs, commits and arrivals.
+  const bool leader = (threadIdx.x & 31) == 0;
+  auto wait_voted = [&](uint32_t bar, uint32_t par) {
+    ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
   };
+  auto wait_full = [&](uint32_t c) { wait_voted(full(c), (c / C::kStages) & 1u); };
   auto release_unused = [&](uint32_t c) {  // a K/V tile this query tile skips
     wait_full(c);                          // its previous phase is then complete
-    if (ok) mbar_arrive(empty(c));
+    if (ok && leader) mbar_arrive(empty(c));
   };
-  if (t == 1) mbar_arrive(sy.turn[0]);  // tile 0 takes the first turn
+  if (t == 1 && leader) mbar_arrive(sy.turn[0]);  // tile 0 takes the first turn
 
   const WorkRange wr = p.range[blockIdx.x];
   const SlotPair sp = p.slots[blockIdx.x];
@@ -367,7 +373,7 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
     const int ne = min(ch.ke, tiles_for<CAUSAL>(ch.rb, t, p));
     const int n_steps = ch.ke - kb;  // both issuers walk the same steps
     if (ne > kb) {
-      ok = ok && wait_phase(bar_q_full, q_uses & 1u, sy, p, kSiteMma);
+      wait_voted(bar_q_full, q_uses & 1u);
       ++q_uses;
     }
     // step s issues O_t += P_t(s-1) V_{s-1} (if kb <= s-1 < ne) and S_t(s) (if s < ne)
@@ -378,10 +384,10 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       const uint32_t ck = kv_count + 2 * (s - kb);          // K_s
       if (do_pv) {
         wait_full(cv);
-        ok = ok && wait_phase(bar_p_ready, pr_par, sy, p, kSiteMma);
+        wait_voted(bar_p_ready, pr_par);
         pr_par ^= 1u;
         if (s == kb + 1) {
-          ok = ok && wait_phase(bar_o_free, of_par, sy, p, kSiteMma);
+          wait_voted(bar_o_free, of_par);
           of_par ^= 1u;
         }
       }
@@ -402,10 +408,11 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
         }
       }
       const uint32_t acc0 = s > kb + 1 ? 1u : 0u;
-      ok = ok && wait_phase(my_turn, turn_par, sy, p, kSiteMma);
+      wait_voted(my_turn, turn_par);
       turn_par ^= 1u;
       if (!ok) break;
       tc_fence_after_sync();
+      if (leader) {
       if (do_pv) {
         constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
 #pragma unroll
@@ -427,13 +434,16 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       if (do_pv) umma_commit(empty(cv));
       if (do_s) umma_commit(empty(ck));
       mbar_arrive(next_turn);
+      }
+      __syncwarp();
       if (!do_pv && s - 1 >= kb) release_unused(cv);
       if (!do_s && s < ch.ke) release_unused(ck);
     }
     kv_count += 2 * n_steps;
   }
   // Every MMA this thread issued must finish before tensor memory is released.
-  umma_commit(sy.drain);
+  if (leader) umma_commit(sy.drain);
+  __syncwarp();
   mbar_wait_bounded(sy.drain, 0, p.wait_limit_ns);
 }
 
@@ -907,7 +917,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
       __syncwarp();
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      if (lane == 0) run_mma<D, CAUSAL>(warp - kMmaWarp, sbase, tmem, sy, p);
+      run_mma<D, CAUSAL>(warp - kMmaWarp, sbase, tmem, sy, p);
       __syncwarp();
     }
   } else {
