@@ -652,7 +652,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   const uint32_t bar_p_ready = t ? sy.p_ready[1] : sy.p_ready[0];
   const uint32_t bar_o_done = t ? sy.o_done[1] : sy.o_done[0];
   const uint32_t bar_o_free = t ? sy.o_free[1] : sy.o_free[0];
-  uint32_t s_par = 0, o_par = 0;
+  uint32_t s_par = 0;
+  uint32_t pv_count = 0;  // P.V products of this tile so far (o_done completes once per product)
   bool ok = true;
 
   const WorkRange wr = p.range[blockIdx.x];
@@ -758,15 +759,17 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       l += sa + sb;
       lq += qa + qb;
 
-      if (j > ch.kb) {
+      if (j > ch.kb && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O_t holds the sum up to tile j-1; bring it to the new reference
-        // maximum where a row moved it (alpha = 1 elsewhere, exact).
-        ok = wait_phase(bar_o_done, o_par, sy, p, kSiteSoftmax);
+        // maximum where a row moved it (alpha = 1 elsewhere, exact).  Only
+        // then is P.V(j-1) waited for: that is its o_done phase, numbered
+        // from the P.V count (the next one cannot complete before this
+        // step's P, so the barrier is never two phases ahead).
+        ok = wait_phase(bar_o_done, (pv_count - 1) & 1u, sy, p, kSiteSoftmax);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        o_par ^= 1u;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        {
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
@@ -788,15 +791,15 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready);  // one arrival per warp
+      ++pv_count;  // P.V(j) follows
     }
     if (!ok) break;
 
     // Epilogue: wait for the last P.V, then O = O_acc / l in bf16 and the
     // natural-log logsumexp L = (m + log2 l) * ln 2.
-    ok = wait_phase(bar_o_done, o_par, sy, p, kSiteSoftmax);
+    ok = wait_phase(bar_o_done, (pv_count - 1) & 1u, sy, p, kSiteSoftmax);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
-    o_par ^= 1u;
     tc_fence_after_sync();
     const float inv_l = 1.f / lq;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
