@@ -733,7 +733,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       const uint64_t qk2 = f2_pack(qk, qk);
       const uint64_t negm2 = f2_pack(-m_use, -m_use);
 
-      uint64_t sum2 = f2_pack(0.f, 0.f), sumq2 = f2_pack(0.f, 0.f);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
+      float lqs[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains for the bf16 sum
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
@@ -749,15 +750,14 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
           sum2 = f2_add(sum2, f2_pack(a, b));
           // also sum the bf16 values the P.V product multiplies, so that
           // O / lq is an exact weighted average of the value rows
-          sumq2 = f2_add(sumq2, f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u)));
+          add_bf16x2_halves(lqs[(i & 1) * 2], lqs[(i & 1) * 2 + 1], pk[i]);
         }
         tmem_st16(tS + c4 * 16, pk);
       }
-      float sa, sb, qa, qb;
+      float sa, sb;
       f2_unpack(sum2, sa, sb);
-      f2_unpack(sumq2, qa, qb);
       l += sa + sb;
-      lq += qa + qb;
+      lq += (lqs[0] + lqs[1]) + (lqs[2] + lqs[3]);
 
       if (j > ch.kb && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O_t holds the sum up to tile j-1; bring it to the new reference

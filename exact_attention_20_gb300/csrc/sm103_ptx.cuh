@@ -373,6 +373,18 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// acc_lo += the low bf16 of pk, acc_hi += the high bf16 of pk (each widened
+// to fp32 exactly, the add rounded to nearest): the row sum of the bf16 P
+// values without unpacking them first.
+__device__ __forceinline__ void add_bf16x2_halves(float& acc_lo, float& acc_hi, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(pk));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
