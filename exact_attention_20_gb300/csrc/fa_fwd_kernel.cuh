@@ -706,58 +706,94 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
           if (c > lim) s[c] = __float_as_uint(-INFINITY);
       }
 
-      // row maximum: four independent chains of 32 columns each
-      float mx[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint32_t* sc = s + 32 * q4;
-        mx[q4] = fmax3(__uint_as_float(sc[0]), __uint_as_float(sc[1]), __uint_as_float(sc[2]));
-      }
-#pragma unroll
-      for (int i = 3; i < 31; i += 2) {
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          mx[q4] = fmax3(mx[q4], __uint_as_float(s[32 * q4 + i]), __uint_as_float(s[32 * q4 + i + 1]));
-      }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) mx[q4] = fmaxf(mx[q4], __uint_as_float(s[32 * q4 + 31]));
-      const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * qk;  // qk > 0: max commutes with the scale
-      float alpha = 1.f;
-      if (m_tile > m_ref + kRescaleThreshold) {  // always taken on the first tile (m_ref = -inf)
-        alpha = ex2_approx(m_ref - m_tile);      // 0 when m_ref = -inf
-        m_ref = m_tile;
-        l *= alpha;
-        lq *= alpha;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const uint64_t qk2 = f2_pack(qk, qk);
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
-
-      uint64_t sum2 = f2_pack(0.f, 0.f);
-      float lqs[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains for the bf16 sum
+      float alpha = 1.f;
+      float sa, sb, lq_tile;
+      // One pass over the tile: exponentials against m_use, P stored to
+      // tensor memory over S, the fp32 and bf16 row sums, and (if asked) the
+      // tile's row maximum from the same values.
+      auto exp_pass = [&](float m_use, bool with_max) -> float {
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t sum2 = f2_pack(0.f, 0.f);
+        float lqs[4] = {0.f, 0.f, 0.f, 0.f};  // four short chains for the bf16 sum
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t pk[16];
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = c4 * 32 + 2 * i;
-          const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
-          float xa, xb;
-          f2_unpack(x, xa, xb);
-          const float a = ex2_approx(xa);
-          const float b = ex2_approx(xb);
-          pk[i] = pack_bf16x2(a, b);
-          sum2 = f2_add(sum2, f2_pack(a, b));
-          // also sum the bf16 values the P.V product multiplies, so that
-          // O / lq is an exact weighted average of the value rows
-          add_bf16x2_halves(lqs[(i & 1) * 2], lqs[(i & 1) * 2 + 1], pk[i]);
+          for (int i = 0; i < 16; ++i) {
+            const int c = c4 * 32 + 2 * i;
+            const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
+            float xa, xb;
+            f2_unpack(x, xa, xb);
+            const float a = ex2_approx(xa);
+            const float b = ex2_approx(xb);
+            pk[i] = pack_bf16x2(a, b);
+            sum2 = f2_add(sum2, f2_pack(a, b));
+            // also sum the bf16 values the P.V product multiplies, so that
+            // O / lq is an exact weighted average of the value rows
+            add_bf16x2_halves(lqs[(i & 1) * 2], lqs[(i & 1) * 2 + 1], pk[i]);
+            if (with_max) mx[c4] = fmax3(mx[c4], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+          }
+          tmem_st16(tS + c4 * 16, pk);
         }
-        tmem_st16(tS + c4 * 16, pk);
+        f2_unpack(sum2, sa, sb);
+        lq_tile = (lqs[0] + lqs[1]) + (lqs[2] + lqs[3]);
+        return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * qk;  // qk > 0: max commutes with the scale
+      };
+      // The row maximum over the tile, alone: four chains of 32 columns.
+      auto row_max = [&]() -> float {
+        float mx[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t* sc = s + 32 * q4;
+          mx[q4] = fmax3(__uint_as_float(sc[0]), __uint_as_float(sc[1]), __uint_as_float(sc[2]));
+        }
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            mx[q4] = fmax3(mx[q4], __uint_as_float(s[32 * q4 + i]), __uint_as_float(s[32 * q4 + i + 1]));
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) mx[q4] = fmaxf(mx[q4], __uint_as_float(s[32 * q4 + 31]));
+        return fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * qk;
+      };
+      if constexpr (CAUSAL) {
+        // The maximum first, then one pass (under the causal mask, whose short
+        // items have many first tiles, this measured faster).
+        const float m_tile = row_max();
+        if (m_tile > m_ref + kRescaleThreshold) {  // always taken on the first tile (m_ref = -inf)
+          alpha = ex2_approx(m_ref - m_tile);      // 0 when m_ref = -inf
+          m_ref = m_tile;
+        }
+        exp_pass(m_ref == -INFINITY ? 0.f : m_ref, false);  // 0: a fully masked row, P = 0
+      } else {
+        // The exponentials are taken against the current reference m_ref
+        // while the tile's own maximum is found in the same pass.  Only if
+        // some row's tile maximum exceeds m_ref by more than
+        // kRescaleThreshold does the warp move that row's reference and take
+        // the pass again, discarding the first one's P and sums (P may then
+        // have overflowed; nothing of it is kept).  A chunk's first tile
+        // (m_ref = -inf) takes its maximum first, so one pass is enough there.
+        if (m_ref == -INFINITY) {
+          m_ref = row_max();
+          alpha = 0.f;  // nothing accumulated before this tile
+        }
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          const float m_tile = exp_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
+          const bool move = m_tile > m_ref + kRescaleThreshold;
+          if (!__any_sync(0xffffffffu, move)) break;
+          if (move) {  // rare: move this row's reference, then the warp takes the pass again
+            alpha = ex2_approx(m_ref - m_tile);
+            m_ref = m_tile;
+          }
+          tmem_st_wait();  // the repeated pass stores P over this one's
+        }
       }
-      float sa, sb;
-      f2_unpack(sum2, sa, sb);
-      l += sa + sb;
-      lq += (lqs[0] + lqs[1]) + (lqs[2] + lqs[3]);
+      l = l * alpha + (sa + sb);
+      lq = lq * alpha + lq_tile;
 
       if (j > ch.kb && __any_sync(0xffffffffu, alpha != 1.f)) {
         // O_t holds the sum up to tile j-1; bring it to the new reference
