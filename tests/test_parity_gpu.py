@@ -105,6 +105,23 @@ def test_max_in_last_key_tile(fa, d, causal):
     assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "max-last")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_max_jumps_in_some_rows_only(fa, d, causal):
+    # even rows see a score jump of about 10-20 (log2 units) in the last key
+    # tile, odd rows see their smallest scores there: within one warp some
+    # rows move their reference maximum and others keep it
+    N = 777
+    q, k, v = make_qkv(1, 2, N, d, seed=78, device=DEV)
+    sign = torch.ones(N, device=DEV)
+    sign[1::2] = -1.0
+    q = (q.float().abs() * sign[None, None, :, None]).to(torch.bfloat16)
+    k = k.clone()
+    k[:, :, N - 5:, :] = 1.5
+    o, lse = run(fa, q, k, v, causal, d ** -0.5)
+    assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "jump-some")
+
+
 @pytest.mark.parametrize("scale", [0.01, 1.0, 3.0])
 def test_scale_values(fa, scale):
     q, k, v = make_qkv(1, 2, 500, 64, seed=3, device=DEV)
