@@ -460,19 +460,22 @@ __device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_
                                              const FwdParams& p) {
   const size_t prow = static_cast<size_t>(ch.slot) * kItemRows + t * kBlockM + row_in_tile;
   if (!empty) {
-    float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
+    // workspace rows are D * 4 bytes in 256-byte aligned slots: 32-byte stores
+    float* dst = p.part_o + prow * D;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
       tmem_ld32_wait(tO + c * 32, o);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float a, b, e, f;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1])), il2), a, b);
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3])), il2), e, f);
-        dst[c * 8 + i] = make_float4(a, b, e, f);
+      for (int i = 0; i < 16; ++i) {
+        float a, b;
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), il2), a, b);
+        o[2 * i] = __float_as_uint(a);
+        o[2 * i + 1] = __float_as_uint(b);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st_global_v8(dst + c * 32 + i * 8, o + i * 8);
     }
   }
   p.part_lse[prow] = lse_part;
@@ -844,6 +847,9 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       // the chunk is the whole item: final O in bf16 and LSE, rows < N only
       const bool store = row < p.N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+      // rows are D * 2 bytes (a multiple of 32), so every row is 32-byte
+      // aligned when O is; the API promises only 16
+      const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -856,9 +862,14 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
           w[i] = pack_bf16x2(lo, hi);
         }
         if (store) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          if (wide) {  // 32-byte stores: half the store instructions, whole sectors
+            st_global_v8(orow + c * 32, w);
+            st_global_v8(orow + c * 32 + 16, w + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
       if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = lse_row;

@@ -373,6 +373,13 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// One 32-byte global store of eight words; `ptr` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // acc_lo += the low bf16 of pk, acc_hi += the high bf16 of pk (each widened
 // to fp32 exactly, the add rounded to nearest): the row sum of the bf16 P
 // values without unpacking them first.

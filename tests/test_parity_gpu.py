@@ -162,6 +162,25 @@ def test_guard_bands_untouched(fa, B, H, N, d, causal):
     assert_close(compare(o, lse, *oracle_full(q, k, v, 0.1, causal)), "guarded")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_output_only_16_byte_aligned(fa, d, causal):
+    # O 16 bytes past a 32-byte boundary: the epilogue must take its 16-byte
+    # store path (the API promises 16-byte alignment only)
+    B, H, N = 2, 3, 300
+    q, k, v = make_qkv(B, H, N, d, seed=12, device=DEV)
+    n_o = B * H * N * d
+    obuf = torch.full((n_o + 64,), -512.0, dtype=torch.bfloat16, device=DEV)
+    assert obuf.data_ptr() % 32 == 0
+    o = obuf[8:8 + n_o].view(B, H, N, d)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=DEV)
+    fa.fa_fwd(q, k, v, o, lse, causal=causal, scale=d ** -0.5)
+    torch.cuda.synchronize()
+    assert (obuf[:8] == -512.0).all() and (obuf[8 + n_o:] == -512.0).all()
+    assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "o16")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_bitwise_deterministic(fa, causal):
     q, k, v = make_workload("B2-H8-N3001-d128-outliers", seed=1, device=DEV)
