@@ -191,10 +191,11 @@ int num_ctas_for(const DeviceInfo* di, int max_ctas) {
 }
 
 // Workspace layout: part O [slots][256][128] fp32, part LSE [slots][256]
-// fp32, then one arrival counter per split item (int, zero between launches).
+// fp32, then the arrival counters: one int per split item, query tile and
+// warp quadrant (zero between launches).
 size_t ws_slots(const DeviceInfo* di) { return 2 * static_cast<size_t>(std::min(di->num_sms, fa::kMaxCtas)); }
 size_t ws_counter_offset(const DeviceInfo* di) { return ws_slots(di) * fa::kItemRows * (128 + 1); }
-size_t ws_bytes(const DeviceInfo* di) { return (ws_counter_offset(di) + fa::kMaxCtas) * sizeof(float); }
+size_t ws_bytes(const DeviceInfo* di) { return (ws_counter_offset(di) + fa::kNumCounters) * sizeof(float); }
 
 void remember_fixed_scratch(DeviceInfo* di, float* ws) {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -209,7 +210,7 @@ float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
     if (w.first == stream) return w.second;
   float* ptr = nullptr;
   if (cudaMalloc(&ptr, ws_bytes(di)) != cudaSuccess) return nullptr;
-  if (cudaMemset(ptr + ws_counter_offset(di), 0, fa::kMaxCtas * sizeof(int)) != cudaSuccess) {
+  if (cudaMemset(ptr + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int)) != cudaSuccess) {
     cudaFree(ptr);
     return nullptr;
   }
@@ -357,7 +358,7 @@ int fa_get_device_status(void* stream) {
     std::vector<float*> areas = di->fixed_scratch;
     for (auto& w : di->workspaces) areas.push_back(w.second);
     for (float* a : areas)
-      if (cudaMemset(a + ws_counter_offset(di), 0, fa::kMaxCtas * sizeof(int)) != cudaSuccess)
+      if (cudaMemset(a + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int)) != cudaSuccess)
         return FA_ERR_LAUNCH;
   }
   return FA_ERR_DEVICE_TIMEOUT;

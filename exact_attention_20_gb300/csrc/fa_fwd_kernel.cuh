@@ -113,7 +113,7 @@ struct FwdParams {
   float qk_scale;          // scale * log2(e)
   unsigned long long wait_limit_ns;
   int starve_kv;           // watchdog self-test: the producer never delivers K/V
-  int* counters;           // workspace: per split item, softmax-warp arrivals (0 between launches)
+  int* counters;           // workspace: per (split item, query tile, warp quadrant) part arrivals (0 between launches)
   WorkRange range[kMaxCtas];
   SlotPair slots[kMaxCtas];
   int merge_item[kMaxCtas];       // per split item: the item
@@ -171,7 +171,8 @@ struct Chunk {
   int kb, ke;
   int slot;   // workspace slot when the chunk is only a part of its item, else -1
   int k;      // its split item, when slot >= 0
-  int todo;   // 0 for the CTA's first chunk, 1 otherwise (its entry in Sync::merge_todo)
+  int todo;   // 0 for the CTA's first chunk, 1 otherwise
+  bool last;  // the CTA's last chunk
 };
 
 __device__ __forceinline__ int num_chunks(const WorkRange& wr) {
@@ -190,6 +191,7 @@ __device__ __forceinline__ Chunk chunk_of(int item, int nkv, const WorkRange& wr
   c.slot = !part ? -1 : (item == wr.item_begin ? sp.first : sp.last);
   c.k = item == wr.item_begin ? sp.k_first : sp.k_last;
   c.todo = item == wr.item_begin ? 0 : 1;
+  c.last = item == wr.item_last;
   return c;
 }
 
@@ -198,7 +200,6 @@ struct Sync {
   uint32_t turn[2];              // hand-over between the two MMA issuers
   uint32_t kv_full0, kv_empty0;  // arrays of kStages barriers, 8 bytes apart
   volatile int* abort_flag;
-  volatile int* merge_todo;  // [2]: split items this CTA completed and merges at its end, else -1
 };
 
 // Bounded wait: true when the phase completed; false if this CTA is aborting
@@ -481,159 +482,146 @@ __device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_
   p.part_lse[prow] = lse_part;
 }
 
-constexpr int kNumSoftmaxThreads = 2 * kBlockM;  // warps 0-7
-constexpr int kNumSoftmaxWarps = kNumSoftmaxThreads / 32;
+constexpr int kCountersPerItem = 2 * 4;                // per query tile and warp quadrant
+constexpr int kNumCounters = kMaxCtas * kCountersPerItem;  // workspace counters (split items <= CTAs)
 
-// A softmax warp has published its rows of one part: it counts its arrival on
-// the item's counter (after making its writes visible device-wide).  The warp
-// whose arrival completes every part of the item (parts x 8 warps) records
-// the item for this CTA to merge at its end.
-__device__ __forceinline__ void arrive_part(const Chunk& ch, int lane, const Sync& sy, const FwdParams& p) {
-  __threadfence();
-  __syncwarp();
-  if (lane == 0) {
-    const int old = atomicAdd(p.counters + ch.k, 1);
-    if (old == p.merge_count[ch.k] * kNumSoftmaxWarps - 1) {
-      __threadfence();
-      sy.merge_todo[ch.todo] = ch.k;
-    }
-  }
-}
-
-// What the merge of one split item needs, copied out of the parameter block
-// so that the merge's stores cannot be taken to alias it.
-struct MergeArgs {
-  __nv_bfloat16* __restrict__ o;
-  float* __restrict__ lse;
-  const float* __restrict__ part_o;
-  const float* __restrict__ part_lse;
-  int N;
-  int rb, bh;
-  int count;
-  int slot[kMaxPartsPerItem];
+// The parts of a split item meet through one counter per (item, query tile,
+// warp quadrant): the warps holding the same 32 rows in each part count
+// their arrivals there.  The warp whose arrival completes the parts merges
+// those 32 rows when its CTA's own work is done, reading its own part from
+// tensor memory when it is still there (the CTA's last chunk: nothing later
+// overwrites that O), and the other parts from the workspace.  In the last
+// chunk a warp first looks at the counter: if every other part is already
+// in, it is the last and publishes nothing.  No warp ever waits for
+// another CTA; the merging warp resets the counter for the next launch.
+struct PartSlots {
+  int n;                       // parts of the item
+  int slot[kMaxPartsPerItem];  // their workspace slots
 };
 
-// The 256 softmax threads merge one split item, every part of which is in
-// the workspace: L = ln sum_r exp(L_r), O = sum_r exp(L_r - L) O_r with the
-// largest L_r subtracted first, written as the final bf16 O and L.  Parts
-// with L_r = -inf weigh 0, and a select (not a product with 0) drops their O,
-// which was never written.
-//
-// Warp w takes rows 32w .. 32w+31 of the item.  Lane l first computes the
-// weights exp(L_r - L) and L of row 32w+l (one exponential per part and one
-// logarithm per row, LSE loads and stores coalesced); then, row after row,
-// the weights are broadcast and the lanes combine the row's O columns
-// (d = 128: lane l has columns 4l..4l+3; d = 64: two rows side by side),
-// with the loads of several rows in flight together.
+struct PendingMerge {
+  int k;          // split item, or -1 for none
+  int own_slot;   // this warp's part's workspace slot (read from there unless in TMEM)
+  bool in_tmem;   // this warp's part is still in tensor memory
+  bool own_empty; // this warp's part has no key for these rows (L = -inf, no O)
+  float inv_l;    // 1 / lq of the own part (the accumulator -> normalised O)
+  float lse_own;  // natural-log logsumexp of the own part
+  int rb, bh;
+};
+
 template <int D>
-__device__ __noinline__ void merge_item(const MergeArgs a) {
-  constexpr int kLanesPerRow = D / 4;
-  constexpr int kRowsPerPass = 32 / kLanesPerRow;  // rows combined side by side
-  constexpr int kPasses = 32 / kRowsPerPass;       // passes over the warp's 32 rows
-  constexpr int kBatch = 8;                        // passes whose loads are in flight together
-  static_assert(kNumSoftmaxWarps * 32 == kItemRows, "one warp per 32 rows");
-  static_assert(kPasses % kBatch == 0, "whole batches of passes");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col4 = lane % kLanesPerRow;
-  const int sub = lane / kLanesPerRow;
-  const int r0 = warp * 32;  // the warp's first row within the item
-  const int row0 = a.rb * kItemRows + r0;
-
-  // weights of row r0 + lane, normalised by their sum
-  float w[kMaxPartsPerItem];
-  {
-    float lr[kMaxPartsPerItem];
-    float m = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < kMaxPartsPerItem; ++q) {
-      lr[q] = q < a.count ? __ldcg(a.part_lse + static_cast<size_t>(a.slot[q]) * kItemRows + r0 + lane)
-                          : -INFINITY;
-      m = fmaxf(m, lr[q]);
-    }
-    float wsum = 0.f;
-#pragma unroll
-    for (int q = 0; q < kMaxPartsPerItem; ++q) {
-      w[q] = lr[q] == -INFINITY ? 0.f : exp2f((lr[q] - m) * 1.4426950408889634f);
-      wsum += w[q];
-    }
-    const float inv = 1.f / wsum;
-#pragma unroll
-    for (int q = 0; q < kMaxPartsPerItem; ++q) w[q] *= inv;
-    if (row0 + lane < a.N) a.lse[static_cast<size_t>(a.bh) * a.N + row0 + lane] = m + logf(wsum);
-  }
-
-  const float4* src[kMaxPartsPerItem];
-#pragma unroll
-  for (int q = 0; q < kMaxPartsPerItem; ++q)
-    src[q] = reinterpret_cast<const float4*>(a.part_o + (static_cast<size_t>(a.slot[q]) * kItemRows + r0) * D);
-  uint2* dst = reinterpret_cast<uint2*>(a.o + (static_cast<size_t>(a.bh) * a.N + row0) * D);
-  auto combine = [&](const float4* x, const float* wr, int rr) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < kMaxPartsPerItem; ++q) {  // weight 0 past the item's parts
-      const bool live = wr[q] != 0.f;
-      acc.x += live ? wr[q] * x[q].x : 0.f;
-      acc.y += live ? wr[q] * x[q].y : 0.f;
-      acc.z += live ? wr[q] * x[q].z : 0.f;
-      acc.w += live ? wr[q] * x[q].w : 0.f;
-    }
-    if (row0 + rr < a.N)
-      dst[rr * (D / 4) + col4] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-  };
-  if (a.count == 2) {
-    for (int b = 0; b < kPasses; b += kBatch) {
-      float4 x[kBatch][2];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int rr = (b + i) * kRowsPerPass + sub;
-        x[i][0] = __ldcg(src[0] + rr * (D / 4) + col4);
-        x[i][1] = __ldcg(src[1] + rr * (D / 4) + col4);
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int rr = (b + i) * kRowsPerPass + sub;
-        const float wr[2] = {__shfl_sync(0xffffffffu, w[0], rr), __shfl_sync(0xffffffffu, w[1], rr)};
-        float4 acc;
-        acc.x = (wr[0] != 0.f ? wr[0] * x[i][0].x : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].x : 0.f);
-        acc.y = (wr[0] != 0.f ? wr[0] * x[i][0].y : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].y : 0.f);
-        acc.z = (wr[0] != 0.f ? wr[0] * x[i][0].z : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].z : 0.f);
-        acc.w = (wr[0] != 0.f ? wr[0] * x[i][0].w : 0.f) + (wr[1] != 0.f ? wr[1] * x[i][1].w : 0.f);
-        if (row0 + rr < a.N)
-          dst[rr * (D / 4) + col4] = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      }
-    }
-  } else {
-    for (int pass = 0; pass < kPasses; ++pass) {
-      const int rr = pass * kRowsPerPass + sub;
-      float4 x[kMaxPartsPerItem];
-      float wr[kMaxPartsPerItem];
-#pragma unroll
-      for (int q = 0; q < kMaxPartsPerItem; ++q) {
-        x[q] = q < a.count ? __ldcg(src[q] + rr * (D / 4) + col4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        wr[q] = __shfl_sync(0xffffffffu, w[q], rr);
-      }
-      combine(x, wr, rr);
+__device__ __forceinline__ PendingMerge part_done(const Chunk& ch, int t, int quad, int lane,
+                                                  int row_in_tile, uint32_t tO, float inv_l,
+                                                  float lse_part, bool empty, const FwdParams& p) {
+  int* ctr = p.counters + ch.k * kCountersPerItem + t * 4 + quad;
+  const int count = p.merge_count[ch.k];
+  PendingMerge pm{-1, ch.slot, ch.last, empty, inv_l, lse_part, ch.rb, ch.bh};
+  if (ch.last) {
+    int seen = 0;
+    if (lane == 0) seen = ld_acquire_gpu(ctr);
+    seen = __shfl_sync(0xffffffffu, seen, 0);
+    if (seen == count - 1) {  // every other part is in: merge, publish nothing
+      pm.k = ch.k;
+      return pm;
     }
   }
+  publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_part, empty, p);
+  __threadfence();
+  __syncwarp();
+  int old = 0;
+  if (lane == 0) old = atomicAdd(ctr, 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == count - 1) pm.k = ch.k;  // arrived last after all
+  return pm;
 }
 
-// Merges split item k (called by the 256 softmax threads) and resets its
-// counter for the next launch: every arrival for the item has happened.
+// Merges one warp's 32 rows (thread = row, as in tensor memory) of a split
+// item: L = ln sum_r exp(L_r), O = sum_r exp(L_r - L) O_r, the largest L_r
+// subtracted first; parts with L_r = -inf weigh 0 and are not read.  The own
+// part comes from tensor memory or its slot; the others from their slots,
+// 32 bytes per load.  Writes the final bf16 O and L of rows < N.
 template <int D>
-__device__ __forceinline__ void merge_split_item(int k, const FwdParams& p) {
-  MergeArgs a;
-  a.o = p.o;
-  a.lse = p.lse;
-  a.part_o = p.part_o;
-  a.part_lse = p.part_lse;
-  a.N = p.N;
-  decode_item(p.merge_item[k], p, a.rb, a.bh);
-  a.count = p.merge_count[k];
-  const int first = p.merge_first[k];
+__device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlots ps, int t, int quad,
+                                        uint32_t tO, int* ctr, __nv_bfloat16* __restrict__ o,
+                                        float* __restrict__ lse, const float* __restrict__ part_o,
+                                        const float* __restrict__ part_lse, int N) {
+  const int lane = threadIdx.x & 31;
+  const int r = t * kBlockM + quad * 32 + lane;  // row within the item
+  const int row = pm.rb * kItemRows + r;
+  // Every lane acquires the counter itself: the other parts' rows were
+  // published (and fenced) before their arrivals were counted.  Then it is
+  // reset for the next launch: every arrival for these rows has happened.
+  (void)ld_acquire_gpu(ctr);
+  __syncwarp();
+  if (lane == 0) *ctr = 0;
+  // the other parts' logsumexps (the own part's is pm.lse_own)
+  float lr[kMaxPartsPerItem];
+  float m = pm.lse_own;
 #pragma unroll
-  for (int q = 0; q < kMaxPartsPerItem; ++q) a.slot[q] = q < a.count ? p.merge_slots[first + q] : 0;
-  if (threadIdx.x == 0) p.counters[k] = 0;
-  merge_item<D>(a);
+  for (int q = 0; q < kMaxPartsPerItem; ++q) {
+    const bool is_other = q < ps.n && ps.slot[q] != pm.own_slot;
+    lr[q] = is_other ? __ldcg(part_lse + static_cast<size_t>(ps.slot[q]) * kItemRows + r) : -INFINITY;
+    m = fmaxf(m, lr[q]);
+  }
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float w_own = pm.lse_own == -INFINITY ? 0.f : exp2f((pm.lse_own - m) * kLog2e);
+  float wsum = w_own;
+  float w[kMaxPartsPerItem];
+#pragma unroll
+  for (int q = 0; q < kMaxPartsPerItem; ++q) {
+    w[q] = lr[q] == -INFINITY ? 0.f : exp2f((lr[q] - m) * kLog2e);
+    wsum += w[q];
+  }
+  const float inv_w = 1.f / wsum;
+  const bool store = row < N;
+  __nv_bfloat16* orow = o + (static_cast<size_t>(pm.bh) * N + (store ? row : 0)) * D;
+  const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  const float* own_row = part_o + (static_cast<size_t>(pm.own_slot) * kItemRows + r) * D;
+  const float f_own = pm.in_tmem ? w_own * pm.inv_l * inv_w : w_own * inv_w;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    float acc[32];
+    if (pm.own_empty) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    } else if (pm.in_tmem) {
+      uint32_t x[32];
+      tmem_ld32_wait(tO + c * 32, x);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(x[i]) * f_own;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ld_global_cg_v8(own_row + c * 32 + i * 8, acc + i * 8);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] *= f_own;
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) {
+      if (w[q] != 0.f) {  // weight 0: never written, never read
+        const float* src = part_o + (static_cast<size_t>(ps.slot[q]) * kItemRows + r) * D + c * 32;
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_global_cg_v8(src + i * 8, x + i * 8);
+        const float wq = w[q] * inv_w;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] += wq * x[i];
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    if (store) {
+      if (wide) {
+        st_global_v8(orow + c * 32, pk);
+        st_global_v8(orow + c * 32 + 16, pk + 8);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+  if (store) lse[static_cast<size_t>(pm.bh) * N + row] = m + logf(wsum);
 }
 
 // ---------------------------------------------------------------------------
@@ -657,6 +645,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   const uint32_t bar_o_free = t ? sy.o_free[1] : sy.o_free[0];
   uint32_t s_par = 0;
   uint32_t pv_count = 0;  // P.V products of this tile so far (o_done completes once per product)
+  // split items this warp's rows complete, merged after the last chunk
+  PendingMerge pend0{-1, 0, false, false, 0.f, 0.f, 0, 0}, pend1 = pend0;
   bool ok = true;
 
   const WorkRange wr = p.range[blockIdx.x];
@@ -674,8 +664,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       // No key tile of this query tile lies in the chunk (past its diagonal).
       // A part still reports its rows, as an empty part: LSE = -inf.
       if (ch.slot >= 0) {
-        publish_part<D>(ch, t, row_in_tile, tO, 0.f, -INFINITY, true, p);
-        arrive_part(ch, lane, sy, p);
+        const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, 0.f, -INFINITY, true, p);
+        if (ch.todo) pend1 = pm; else pend0 = pm;
       }
       continue;
     }
@@ -875,12 +865,28 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = lse_row;
     } else {
       // a part of the item: merged once every part is in (merge_item)
-      publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_row, false, p);
-      arrive_part(ch, lane, sy, p);
+      const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, inv_l, lse_row, false, p);
+      if (ch.todo) pend1 = pm; else pend0 = pm;
     }
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_o_free);  // one arrival per warp
+  }
+  // The merges of the split items these rows completed.  The last chunk's O
+  // is still in tensor memory: no product of this tile follows it.
+  if (!ok || *sy.abort_flag) return;
+#pragma unroll 1
+  for (int i = 0; i < 2; ++i) {
+    const PendingMerge pm = i ? pend1 : pend0;
+    if (pm.k < 0) continue;
+    PartSlots ps;
+    ps.n = p.merge_count[pm.k];
+    const int first = p.merge_first[pm.k];
+#pragma unroll
+    for (int q = 0; q < kMaxPartsPerItem; ++q) ps.slot[q] = q < ps.n ? p.merge_slots[first + q] : -1;
+    tc_fence_after_sync();
+    merge_rows<D>(pm, ps, t, quad, tO, p.counters + pm.k * kCountersPerItem + t * 4 + quad, p.o, p.lse, p.part_o,
+                  p.part_lse, p.N);
   }
 }
 
@@ -924,7 +930,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
-  sy.merge_todo = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 8);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -943,8 +948,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(sy.turn[0], 1);
     mbar_init(sy.turn[1], 1);
     *sy.abort_flag = 0;
-    sy.merge_todo[0] = -1;
-    sy.merge_todo[1] = -1;
     fence_barrier_init();
   }
   if (warp == kLoadWarp && lane == 0) {
@@ -973,15 +976,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
     run_softmax<D, CAUSAL>(warp >> 2, tmem, sy, p);
-    // The softmax warps merge the split items this CTA completed, after all
-    // their own work (merge_todo is final once all eight have passed here).
-    named_bar_sync(1, kNumSoftmaxThreads);
-    if (*sy.abort_flag == 0) {
-      for (int i = 0; i < 2; ++i) {
-        const int k = sy.merge_todo[i];
-        if (k >= 0) merge_split_item<D>(k, p);
-      }
-    }
   }
 
   tc_fence_before_sync();

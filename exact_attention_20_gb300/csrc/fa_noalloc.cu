@@ -19,9 +19,10 @@
 namespace {
 
 // Room for the split-item workspace of up to 160 CTAs at d <= 128:
-// 2 parts per CTA x 256 rows x (128 O values + 1 logsumexp) fp32, then 256
-// arrival counters (one per split item).
-constexpr size_t kScratchFloats = static_cast<size_t>(FA_NOALLOC_MAX_CTAS) * 2 * 256 * 129 + 256;
+// 2 parts per CTA x 256 rows x (128 O values + 1 logsumexp) fp32, then 2048
+// arrival counters (8 per split item: query tile x warp quadrant; at most
+// 256 split items).
+constexpr size_t kScratchFloats = static_cast<size_t>(FA_NOALLOC_MAX_CTAS) * 2 * 256 * 129 + 2048;
 static_assert(kScratchFloats * sizeof(float) == FA_NOALLOC_SCRATCH_BYTES,
               "the header states the scratch size");
 

@@ -20,7 +20,7 @@
  *     The caller owns every buffer it passes.  The library's own device
  *     memory is a status word per device (static) and, per stream, one
  *     workspace of 2 x (SMs, at most 256) x 256 x 129 fp32 values (about
- *     40 MB on a GB300) plus 256 counters for the parts of split work
+ *     40 MB on a GB300) plus 2048 counters for the parts of split work
  *     items, allocated (and its counters zeroed) on the
  *     first fa_fwd on that stream that splits an item and kept until the
  *     process exits.  Calls on one stream reuse its workspace in stream
@@ -93,8 +93,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * cudaMalloc/cudaFree blocking on work queued on other streams.
  *
  *   - Limit: the scratch holds the workspace of up to FA_NOALLOC_MAX_CTAS
- *     CTAs (two parts of 256 rows x 129 fp32 each per CTA, and one arrival
- *     counter per split item); the work plan
+ *     CTAs (two parts of 256 rows x 129 fp32 each per CTA, and eight arrival
+ *     counters per split item); the work plan
  *     uses one CTA per SM.  On a device with more SMs than that, a call
  *     that splits items returns FA_ERR_SCRATCH and launches nothing.
  *     Problem sizes are limited as for fa_fwd.
@@ -116,7 +116,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  * FA_ERR_SCRATCH).
  */
 #define FA_NOALLOC_MAX_CTAS 160
-#define FA_NOALLOC_SCRATCH_BYTES ((160u * 2u * 256u * 129u + 256u) * 4u) /* 42,271,744 bytes */
+#define FA_NOALLOC_SCRATCH_BYTES ((160u * 2u * 256u * 129u + 2048u) * 4u) /* 42,278,912 bytes */
 int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                    int B, int H, int N, int d, int causal, float scale, void* stream);
 

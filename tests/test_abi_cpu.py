@@ -152,4 +152,4 @@ def test_noalloc_scratch_size_is_stated_in_the_header():
         text = f.read()
     ctas = int(_re.search(r"#define FA_NOALLOC_MAX_CTAS (\d+)", text).group(1))
     assert ctas == 160
-    assert "42,271,744 bytes" in text and (ctas * 2 * 256 * 129 + 256) * 4 == 42271744
+    assert "42,278,912 bytes" in text and (ctas * 2 * 256 * 129 + 2048) * 4 == 42278912
