@@ -242,6 +242,19 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
     decode_item(item, p, rb, bh);
     const int nkv = item_steps<CAUSAL>(rb, p);
     const Chunk ch = chunk_of(item, nkv, wr, sp, p);
+    if (ch.slot >= 0 && ch.last) {
+      // The CTA's last chunk is a part of a split item: its warps will most
+      // likely merge the item when the chunk ends, and the other parts were
+      // published long ago, when their CTAs started.  Bring them back into
+      // L2 while the chunk runs.
+      const int first = p.merge_first[ch.k], count = p.merge_count[ch.k];
+      for (int i = 0; i < count; ++i) {
+        const int slot = p.merge_slots[first + i];
+        if (slot == ch.slot) continue;
+        prefetch_l2_bulk(p.part_o + static_cast<size_t>(slot) * kItemRows * D, kItemRows * D * 4);
+        prefetch_l2_bulk(p.part_lse + static_cast<size_t>(slot) * kItemRows, kItemRows * 4);
+      }
+    }
     for (int t = 0; t < kQTiles && ok; ++t) {
       if (min(ch.ke, tiles_for<CAUSAL>(rb, t, p)) <= ch.kb) continue;  // no tile of its own here
       ok = wait_phase(sy.q_empty[t], (q_loads[t] & 1u) ^ 1u, sy, p, kSiteProducer);
@@ -578,46 +591,52 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
   const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   const float* own_row = part_o + (static_cast<size_t>(pm.own_slot) * kItemRows + r) * D;
   const float f_own = pm.in_tmem ? w_own * pm.inv_l * inv_w : w_own * inv_w;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    float acc[32];
+  // 64 columns at a time, each part's loads of them in flight together
+  constexpr int kHalf = D < 64 ? D : 64;
+#pragma unroll 1
+  for (int h = 0; h < D / kHalf; ++h) {
+    float acc[kHalf];
     if (pm.own_empty) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      for (int i = 0; i < kHalf; ++i) acc[i] = 0.f;
     } else if (pm.in_tmem) {
-      uint32_t x[32];
-      tmem_ld32_wait(tO + c * 32, x);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(x[i]) * f_own;
+      for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t x[32];
+        tmem_ld32_wait(tO + h * kHalf + c * 32, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __uint_as_float(x[i]) * f_own;
+      }
     } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ld_global_cg_v8(own_row + c * 32 + i * 8, acc + i * 8);
+      for (int i = 0; i < kHalf / 8; ++i) ld_global_cg_v8(own_row + h * kHalf + i * 8, acc + i * 8);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] *= f_own;
+      for (int i = 0; i < kHalf; ++i) acc[i] *= f_own;
     }
 #pragma unroll
     for (int q = 0; q < kMaxPartsPerItem; ++q) {
       if (w[q] != 0.f) {  // weight 0: never written, never read
-        const float* src = part_o + (static_cast<size_t>(ps.slot[q]) * kItemRows + r) * D + c * 32;
-        float x[32];
+        const float* src = part_o + (static_cast<size_t>(ps.slot[q]) * kItemRows + r) * D + h * kHalf;
+        float x[kHalf];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ld_global_cg_v8(src + i * 8, x + i * 8);
+        for (int i = 0; i < kHalf / 8; ++i) ld_global_cg_v8(src + i * 8, x + i * 8);
         const float wq = w[q] * inv_w;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] += wq * x[i];
+        for (int i = 0; i < kHalf; ++i) acc[i] += wq * x[i];
       }
     }
-    uint32_t pk[16];
+    uint32_t pk[kHalf / 2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    for (int i = 0; i < kHalf / 2; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
     if (store) {
+      __nv_bfloat16* dst = orow + h * kHalf;
       if (wide) {
-        st_global_v8(orow + c * 32, pk);
-        st_global_v8(orow + c * 32 + 16, pk + 8);
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < kHalf / 16; ++i) st_global_v8(dst + i * 16, pk + i * 8);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kHalf / 8; ++i)
+          reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
   }

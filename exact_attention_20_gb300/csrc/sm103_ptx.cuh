@@ -73,6 +73,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ---------------------------------------------------------------------------
+// Bulk prefetch of [ptr, ptr + bytes) from global memory into L2 (ptr and
+// bytes multiples of 16).  A hint: nothing to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
