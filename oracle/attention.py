@@ -121,7 +121,7 @@ def _f64(a) -> np.ndarray:
 
 
 def _visible(n_keys: int, rows: np.ndarray, causal: bool) -> np.ndarray:
-    """Boolean [len(rows), n_keys]: key j is visible to query i iff j < N and (not causal or j <= i)."""
+    """Boolean [len(rows), n_keys]: key j is visible to query i iff j < N_k and (not causal or j <= i)."""
     j = np.arange(n_keys)[None, :]
     if causal:
         return j <= rows[:, None]
@@ -131,7 +131,7 @@ def _visible(n_keys: int, rows: np.ndarray, causal: bool) -> np.ndarray:
 def _head_rows(q, k, v, scale: float, causal: bool, rows: np.ndarray):
     """Definition for a set of query rows of one head.
 
-    q: [N, d], k: [N, d], v: [N, d] (float64); rows: int indices into q.
+    q: [N_q, d], k: [N_k, d], v: [N_k, d_v] (float64); rows: int indices into q.
     Returns (O [len(rows), d], LSE [len(rows)]) in float64.
     """
     s = scale * (q[rows] @ k.T)                      # scores s_ij = scale * q_i . k_j
@@ -158,28 +158,33 @@ def attention_weights(q, k, scale: float, causal: bool) -> np.ndarray:
 
 
 def attention(q, k, v, scale: float, causal: bool, row_block: int = 256):
-    """O and LSE for q, k shaped [..., N, d] and v [..., N, d_v] (leading axes are independent heads).
+    """O and LSE for q [..., N_q, d], k [..., N_k, d] and v [..., N_k, d_v].
 
-    Returns (O float64 [..., N, d_v], LSE float64 [..., N]).  S is materialised
-    ``row_block`` query rows at a time so that long sequences fit in host
-    memory; every row is still computed by the plain definition.
+    Leading axes are independent heads.  N_q and N_k may differ; causal then
+    keeps key j for query i when j <= i, the top-left mask ("How to profile
+    and optimise kernels", Round 4: non-square causal attention is checked
+    against an explicit top-left mask).  Returns (O float64 [..., N_q, d_v],
+    LSE float64 [..., N_q]).  S is materialised ``row_block`` query rows at a
+    time so that long sequences fit in host memory; every row is still
+    computed by the plain definition.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
-    if q.shape != k.shape or v.shape[:-1] != k.shape[:-1]:
-        raise ValueError("q and k must share one shape [..., N, d]; v must be [..., N, d_v]")
+    if q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1] or v.shape[:-1] != k.shape[:-1]:
+        raise ValueError("q must be [..., N_q, d], k [..., N_k, d] and v [..., N_k, d_v]")
     lead = q.shape[:-2]
-    n, d = q.shape[-2:]
+    n_q, d = q.shape[-2:]
+    n_k = k.shape[-2]
     dv = v.shape[-1]
-    qf = q.reshape(-1, n, d)
-    kf = k.reshape(-1, n, d)
-    vf = v.reshape(-1, n, dv)
-    o = np.empty((qf.shape[0], n, dv))
+    qf = q.reshape(-1, n_q, d)
+    kf = k.reshape(-1, n_k, d)
+    vf = v.reshape(-1, n_k, dv)
+    o = np.empty((qf.shape[0], n_q, dv))
     lse = np.empty(qf.shape[:2], dtype=np.float64)
     for h in range(qf.shape[0]):
-        for r0 in range(0, n, row_block):
-            rows = np.arange(r0, min(n, r0 + row_block))
+        for r0 in range(0, n_q, row_block):
+            rows = np.arange(r0, min(n_q, r0 + row_block))
             o[h, rows], lse[h, rows] = _head_rows(qf[h], kf[h], vf[h], scale, causal, rows)
-    return o.reshape(*lead, n, dv), lse.reshape(*lead, n)
+    return o.reshape(*lead, n_q, dv), lse.reshape(*lead, n_q)
 
 
 def attention_rows(q_head, k_head, v_head, scale: float, causal: bool, rows):

@@ -24,6 +24,7 @@ MUTATIONS = {
     "scale_dropped": ("s = scale * (q[rows] @ k.T)", "s = (q[rows] @ k.T)"),
     "causal_off_by_one": ("return j <= rows[:, None]", "return j < rows[:, None]"),
     "causal_flipped": ("return j <= rows[:, None]", "return j >= rows[:, None]"),
+    "causal_bottom_right": ("return j <= rows[:, None]", "return j <= rows[:, None] + (n_keys - rows.size)"),
     "max_shift_dropped": ("e = np.exp(s - m)  ", "e = np.exp(s)  "),
     "sum_wrong_axis": ("l = np.sum(e, axis=1, keepdims=True)", "l = np.sum(e, axis=0, keepdims=True)"),
     "no_normalisation": ("o = (e @ v) / l  ", "o = (e @ v)  "),

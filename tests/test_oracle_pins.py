@@ -147,6 +147,40 @@ def test_brute_force_tiny(n, d, causal):
     np.testing.assert_allclose(lse, lse_b, rtol=0, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n_q,n_k", [(1, 7), (3, 8), (8, 3), (5, 1), (2, 9), (6, 4)])
+def test_brute_force_rectangular(n_q, n_k, causal):
+    # N_q != N_k with the top-left causal mask (key j visible to query i iff
+    # j <= i), "How to profile and optimise kernels", Round 4
+    rng = np.random.default_rng(100 * n_q + n_k)
+    q = rng.normal(size=(n_q, 3))
+    k, v = rng.normal(size=(n_k, 3)), rng.normal(size=(n_k, 2))
+    o_b, lse_b = _brute(q.tolist(), k.tolist(), v.tolist(), 0.6, causal)
+    o, lse = oracle.attention(q, k, v, 0.6, causal)
+    np.testing.assert_allclose(o, o_b, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_b, rtol=0, atol=1e-13)
+
+
+def test_rectangular_causal_limits():
+    # top-left causal: with N_q < N_k the keys from N_q on are never visible,
+    # so dropping them changes nothing; with N_q > N_k every row from N_k - 1
+    # on sees every key, as without the mask
+    rng = np.random.default_rng(31)
+    q = rng.normal(size=(2, 5, 4))
+    k, v = rng.normal(size=(2, 12, 4)), rng.normal(size=(2, 12, 4))
+    o, lse = oracle.attention(q, k, v, 0.5, True)
+    o_t, lse_t = oracle.attention(q, k[:, :5], v[:, :5], 0.5, True)
+    np.testing.assert_allclose(o, o_t, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_t, rtol=0, atol=1e-14)
+    q2 = rng.normal(size=(2, 12, 4))
+    k2, v2 = rng.normal(size=(2, 5, 4)), rng.normal(size=(2, 5, 4))
+    o_c, lse_c = oracle.attention(q2, k2, v2, 0.5, True)
+    o_n, lse_n = oracle.attention(q2, k2, v2, 0.5, False)
+    np.testing.assert_allclose(o_c[:, 4:], o_n[:, 4:], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse_c[:, 4:], lse_n[:, 4:], rtol=0, atol=1e-14)
+    assert np.abs(o_c[:, :4] - o_n[:, :4]).max() > 1e-3  # the mask does act on the first rows
+
+
 def test_brute_force_batched_heads_keep_their_own_data():
     rng = np.random.default_rng(7)
     q, k, v = (rng.normal(size=(2, 3, 5, 4)) for _ in range(3))
