@@ -358,6 +358,68 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+DECODE_SHAPES = [(1, 32, 1, 32768, 128), (1, 32, 128, 32768, 128)]  # B, H, Nq, Nk, d
+
+
+def run_decode(args):
+    """Few query rows over long keys (fa_fwd_rect, non-causal): HBM-bound.
+
+    The algorithmic bytes are Q, K, V read once and O, LSE written once; the
+    useful FLOPs (4 B H Nq Nk d) are negligible.  The value is the bytes per
+    second of the one-query-row shape against the measured copy bandwidth.
+    """
+    from exact_attention_20_gb300 import build as fa_build
+
+    fa_build.build()
+    from exact_attention_20_gb300 import fa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        hbm = json.load(f).get("hbm_gbs", 6800.0)
+    sampler = ClockSampler(0)
+    sampler.start()
+    per_shape = {}
+    for B, H, Nq, Nk, d in DECODE_SHAPES:
+        q, _, _ = make_qkv(B, H, Nq, d, seed=1, device=dev)
+        _, k, v = make_qkv(B, H, Nk, d, seed=2, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            fa.fa_fwd_rect(q, k, v, o, lse, scale=d ** -0.5)
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        sampler.mark("t0")
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fa.fa_fwd_rect(q, k, v, o, lse, scale=d ** -0.5)
+            e1.record()
+        torch.cuda.synchronize(dev)
+        sampler.mark("t1")
+        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        nbytes = B * H * (2 * Nq * d * 2 + 2 * Nk * d * 2 + Nq * 4)
+        grid, nsplit = fa.plan(B, H, Nq, d, False, n_keys=Nk)
+        per_shape[f"B{B}-H{H}-Nq{Nq}-Nk{Nk}-d{d}"] = {
+            "ms": ms, "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+            "algorithmic_bytes": nbytes, "useful_tflops": 4.0 * B * H * Nq * Nk * d / (ms * 1e-3) / 1e12,
+            "ctas": grid, "split_items": nsplit}
+    clocks = sampler.stop()
+    first = next(iter(per_shape.values()))
+    print(json.dumps({
+        "metric": "attn fwd decode: algorithmic bytes per second, few query rows over 32768 keys (bf16, non-causal)",
+        "value": first["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode", "shapes": list(per_shape),
+                   "l2": "flushed before every call (256 MiB write, outside the events)"},
+        "per_shape": per_shape,
+        "roofline": {"bound": "hbm", "achieved": first["gbs"], "peak": hbm, "unit": "GB/s",
+                     "frac": first["gbs"] / hbm, "peak_kind": "measured copy bandwidth"},
+        "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,6 +429,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-heads", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true",
+                    help="the few-query-rows shapes through fa_fwd_rect (HBM-bound), "
+                         "instead of the headline step")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed kernel steps (for profiler runs): no clock sampling, "
                          "no end-to-end leg, no CPU baseline, no one-second warm-up floor")
@@ -375,6 +440,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode:
+        run_decode(args)
     else:
         run_ours(args)
 

@@ -45,25 +45,29 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// Host-only checks, done before any CUDA call.
+// Host-only checks, done before any CUDA call.  q and o hold Nq rows per
+// (b, h), k and v hold Nk.
 int check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
-               int H, int N, int d, int causal, float scale) {
-  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+               int H, int Nq, int Nk, int d, int causal, float scale) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  const long long elems = static_cast<long long>(B) * H * N * d;
-  if (elems >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  const long long elems_q = static_cast<long long>(B) * H * Nq * d;
+  const long long elems_k = static_cast<long long>(B) * H * Nk * d;
+  if (elems_q >= (1ll << 31) || elems_k >= (1ll << 31)) return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return FA_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
-  const size_t tb = static_cast<size_t>(elems) * 2;
-  const size_t lb = static_cast<size_t>(B) * H * N * 4;
-  for (const void* in : {q, k, v}) {
-    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_ALIAS;
+  const size_t qb = static_cast<size_t>(elems_q) * 2;  // q and o
+  const size_t kb = static_cast<size_t>(elems_k) * 2;  // k and v
+  const size_t lb = static_cast<size_t>(B) * H * Nq * 4;
+  if (overlaps(o, qb, q, qb) || overlaps(lse, lb, q, qb)) return FA_ERR_ALIAS;
+  for (const void* in : {k, v}) {
+    if (overlaps(o, qb, in, kb) || overlaps(lse, lb, in, kb)) return FA_ERR_ALIAS;
   }
-  if (overlaps(o, tb, lse, lb)) return FA_ERR_ALIAS;
+  if (overlaps(o, qb, lse, lb)) return FA_ERR_ALIAS;
   return FA_OK;
 }
 
@@ -88,13 +92,13 @@ DeviceInfo* device_info(int* dev_out) {
 
 // Host copy of the kernel's work accounting (decode_item, tiles_for, item_steps).
 struct PlanShape {
-  int N, BH, nkt, nrb;
+  int Nq, BH, nkt, nrb;  // query rows, B*H, key tiles, row blocks
   bool causal;
 };
 
 int host_tiles_for(const PlanShape& s, int rb, int t) {
   const int r0 = rb * fa::kItemRows + t * fa::kBlockM;
-  if (r0 >= s.N) return 0;
+  if (r0 >= s.Nq) return 0;
   return s.causal ? std::min(r0 / fa::kBlockN + 1, s.nkt) : s.nkt;
 }
 
@@ -106,7 +110,8 @@ int host_item_steps(const PlanShape& s, int item) {
 
 // Splits the concatenated steps of all items into `grid` equal contiguous
 // ranges (one per CTA) and lists the items that end up in several parts.
-// With no more items than SMs, each CTA takes one whole item instead.
+// With no more items than SMs the keys are split only when every CTA keeps
+// at least 16 steps; otherwise each CTA takes one whole item.
 // Returns false when a split would need more parts per item than the merge
 // takes; the caller then uses whole items.  num_split = split items.
 bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams& p, int& grid,
@@ -114,11 +119,21 @@ bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams
   const int items = s.BH * s.nrb;
   num_split = 0;
   int nslots = 0;
-  if (!allow_split || items <= num_ctas) return false;
-  grid = num_ctas;
+  if (!allow_split) return false;
   std::vector<long long> start(items + 1, 0);
   for (int i = 0; i < items; ++i) start[i + 1] = start[i] + host_item_steps(s, i);
   const long long W = start[items];
+  grid = num_ctas;
+  if (items <= num_ctas) {
+    // Few items (few query rows over many keys, the decode shape): their
+    // keys are split over more CTAs while each CTA keeps enough steps to
+    // amortise the merge, and no item goes into more parts than it takes.
+    constexpr long long kMinStepsPerCta = 16;
+    grid = static_cast<int>(std::min<long long>(
+        {static_cast<long long>(num_ctas), W / kMinStepsPerCta,
+         static_cast<long long>(items) * (fa::kMaxPartsPerItem - 1)}));
+    if (grid <= items) return false;
+  }
   auto locate = [&](long long g, int& item, int& step) {
     item = static_cast<int>(std::upper_bound(start.begin(), start.end(), g) - start.begin()) - 1;
     step = static_cast<int>(g - start[item]);
@@ -219,14 +234,14 @@ float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
 }
 
 template <int D, bool CAUSAL>
-int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk,
            float scale, cudaStream_t stream, DeviceInfo* di, unsigned long long wait_limit_ns,
            int starve_kv, int max_ctas, const fa_internal::Scratch& fixed) {
   using C = fa::Cfg<D>;
   CUtensorMap tq, tk, tv;
-  if (!fa::encode_bf16_3d(&tq, q, D, N, BH, 64, fa::kBlockM) ||
-      !fa::encode_bf16_3d(&tk, k, D, N, BH, 64, fa::kBlockN) ||
-      !fa::encode_bf16_3d(&tv, v, D, N, BH, 64, fa::kBlockN))
+  if (!fa::encode_bf16_3d(&tq, q, D, Nq, BH, 64, fa::kBlockM) ||
+      !fa::encode_bf16_3d(&tk, k, D, Nk, BH, 64, fa::kBlockN) ||
+      !fa::encode_bf16_3d(&tv, v, D, Nk, BH, 64, fa::kBlockN))
     return FA_ERR_LAUNCH;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -245,17 +260,18 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.status = di->status;
-  p.N = N;
+  p.Nq = Nq;
+  p.Nk = Nk;
   p.BH = BH;
-  p.n_key_tiles = (N + fa::kBlockN - 1) / fa::kBlockN;
-  p.n_row_blocks = (N + fa::kItemRows - 1) / fa::kItemRows;
+  p.n_key_tiles = (Nk + fa::kBlockN - 1) / fa::kBlockN;
+  p.n_row_blocks = (Nq + fa::kItemRows - 1) / fa::kItemRows;
   p.num_items = BH * p.n_row_blocks;
   p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit_ns = wait_limit_ns;
   p.starve_kv = starve_kv;
   p.part_o = nullptr;
   p.part_lse = nullptr;
-  const PlanShape shape{N, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
+  const PlanShape shape{Nq, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
   int num_split = 0;
   const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, num_split);
   p.counters = nullptr;
@@ -280,10 +296,11 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   return FA_OK;
 }
 
-int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-             int d, int causal, float scale, cudaStream_t stream, unsigned long long wait_limit_ns,
-             int starve_kv, int max_ctas, const fa_internal::Scratch& fixed) {
-  int rc = check_args(q, k, v, o, lse, B, H, N, d, causal, scale);
+int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+             int Nk, int d, int causal, float scale, cudaStream_t stream,
+             unsigned long long wait_limit_ns, int starve_kv, int max_ctas,
+             const fa_internal::Scratch& fixed) {
+  int rc = check_args(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale);
   if (rc != FA_OK) return rc;
   int dev = 0;
   DeviceInfo* di = device_info(&dev);
@@ -291,10 +308,10 @@ int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!di->supported) return FA_ERR_DEVICE;
   const int BH = B * H;
   if (d == 128)
-    return causal ? launch<128, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
-                  : launch<128, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
-  return causal ? launch<64, true>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
-                : launch<64, false>(q, k, v, o, lse, BH, N, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
+    return causal ? launch<128, true>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
+                  : launch<128, false>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
+  return causal ? launch<64, true>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
+                : launch<64, false>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
 }
 
 }  // namespace
@@ -303,12 +320,12 @@ namespace fa_internal {
 
 int check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    int B, int H, int N, int d, int causal, float scale) {
-  return check_args(q, k, v, o, lse, B, H, N, d, causal, scale);
+  return check_args(q, k, v, o, lse, B, H, N, N, d, causal, scale);
 }
 
 int fwd_with_scratch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int N, int d, int causal, float scale, void* stream, const Scratch& scratch) {
-  return dispatch(q, k, v, o, lse, B, H, N, d, causal, scale, static_cast<cudaStream_t>(stream),
+  return dispatch(q, k, v, o, lse, B, H, N, N, d, causal, scale, static_cast<cudaStream_t>(stream),
                   kWaitLimitNs, 0, 0, scratch);
 }
 
@@ -318,7 +335,13 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, int causal, float scale, void* stream) {
-  return dispatch(q, k, v, o, lse, B, H, N, d, causal, scale, static_cast<cudaStream_t>(stream),
+  return dispatch(q, k, v, o, lse, B, H, N, N, d, causal, scale, static_cast<cudaStream_t>(stream),
+                  kWaitLimitNs, 0, 0, fa_internal::Scratch{});
+}
+
+int fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Nq, int Nk, int d, int causal, float scale, void* stream) {
+  return dispatch(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, static_cast<cudaStream_t>(stream),
                   kWaitLimitNs, 0, 0, fa_internal::Scratch{});
 }
 
@@ -368,28 +391,31 @@ int fa_watchdog_selftest(const void* q, const void* k, const void* v, void* o, f
                          int limit_ms, void* stream) {
   if (limit_ms < 1 || limit_ms > 10000) return FA_ERR_INVALID_ARG;
   const unsigned long long lim = static_cast<unsigned long long>(limit_ms) * 1000000ull;
-  int rc = dispatch(q, k, v, o, lse, 1, 1, 128, 64, 0, 0.125f, static_cast<cudaStream_t>(stream),
+  int rc = dispatch(q, k, v, o, lse, 1, 1, 128, 128, 64, 0, 0.125f, static_cast<cudaStream_t>(stream),
                     lim, /*starve_kv=*/1, /*max_ctas=*/1, fa_internal::Scratch{});
   if (rc != FA_OK) return rc;
   return fa_get_device_status(stream);
 }
 
-int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_split_items) {
+int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
+                int* num_split_items) {
   if (num_ctas == nullptr || num_split_items == nullptr) return FA_ERR_NULL;
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1))
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1))
     return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H * N * d >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * Nq * d >= (1ll << 31) ||
+      static_cast<long long>(B) * H * Nk * d >= (1ll << 31))
+    return FA_ERR_INVALID_ARG;
   int dev = 0;
   DeviceInfo* di = device_info(&dev);
   if (di == nullptr) return FA_ERR_LAUNCH;
   if (!di->supported) return FA_ERR_DEVICE;
   const int BH = B * H;
-  const int nkt = (N + fa::kBlockN - 1) / fa::kBlockN;
-  const int nrb = (N + fa::kItemRows - 1) / fa::kItemRows;
+  const int nkt = (Nk + fa::kBlockN - 1) / fa::kBlockN;
+  const int nrb = (Nq + fa::kItemRows - 1) / fa::kItemRows;
   static fa::FwdParams p;
   int num_split = 0;
   std::lock_guard<std::mutex> plan_lock(g_plan_mu);
-  *num_ctas = plan_launch(PlanShape{N, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p,
+  *num_ctas = plan_launch(PlanShape{Nq, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p,
                           num_split);
   *num_split_items = num_split;
   return FA_OK;

@@ -105,7 +105,8 @@ struct FwdParams {
   int* status;             // device status word (0 = ok)
   float* part_o;           // workspace: [slot][256][D] fp32, O of a part, normalised within it
   float* part_lse;         // workspace: [slot][256] fp32, the part's natural-log logsumexp
-  int N;
+  int Nq;                  // query rows (of O and LSE)
+  int Nk;                  // keys (of K and V)
   int BH;
   int n_key_tiles;         // ceil(N / 128)
   int n_row_blocks;        // ceil(N / 256)
@@ -150,11 +151,12 @@ __device__ __forceinline__ void decode_item(int item, const FwdParams& p, int& r
 }
 
 // Number of key tiles query tile t of row block rb visits (0 if the tile
-// lies beyond N).
+// lies beyond the last query row).  Causal is the top-left mask: key j for
+// query i iff j <= i, so rows past the last key see every key tile.
 template <bool CAUSAL>
 __device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
   const int r0 = rb * kItemRows + t * kBlockM;
-  if (r0 >= p.N) return 0;
+  if (r0 >= p.Nq) return 0;
   if (CAUSAL) return min(r0 / kBlockN + 1, p.n_key_tiles);
   return p.n_key_tiles;
 }
@@ -552,12 +554,12 @@ __device__ __forceinline__ PendingMerge part_done(const Chunk& ch, int t, int qu
 // item: L = ln sum_r exp(L_r), O = sum_r exp(L_r - L) O_r, the largest L_r
 // subtracted first; parts with L_r = -inf weigh 0 and are not read.  The own
 // part comes from tensor memory or its slot; the others from their slots,
-// 32 bytes per load.  Writes the final bf16 O and L of rows < N.
+// 32 bytes per load.  Writes the final bf16 O and L of rows < Nq.
 template <int D>
 __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlots ps, int t, int quad,
                                         uint32_t tO, int* ctr, __nv_bfloat16* __restrict__ o,
                                         float* __restrict__ lse, const float* __restrict__ part_o,
-                                        const float* __restrict__ part_lse, int N) {
+                                        const float* __restrict__ part_lse, int Nq) {
   const int lane = threadIdx.x & 31;
   const int r = t * kBlockM + quad * 32 + lane;  // row within the item
   const int row = pm.rb * kItemRows + r;
@@ -586,8 +588,8 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
     wsum += w[q];
   }
   const float inv_w = 1.f / wsum;
-  const bool store = row < N;
-  __nv_bfloat16* orow = o + (static_cast<size_t>(pm.bh) * N + (store ? row : 0)) * D;
+  const bool store = row < Nq;
+  __nv_bfloat16* orow = o + (static_cast<size_t>(pm.bh) * Nq + (store ? row : 0)) * D;
   const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   const float* own_row = part_o + (static_cast<size_t>(pm.own_slot) * kItemRows + r) * D;
   const float f_own = pm.in_tmem ? w_own * pm.inv_l * inv_w : w_own * inv_w;
@@ -640,7 +642,7 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
       }
     }
   }
-  if (store) lse[static_cast<size_t>(pm.bh) * N + row] = m + logf(wsum);
+  if (store) lse[static_cast<size_t>(pm.bh) * Nq + row] = m + logf(wsum);
 }
 
 // ---------------------------------------------------------------------------
@@ -656,7 +658,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   const uint32_t tS = tmem + lane_off + t * 128;
   const uint32_t tO = tmem + lane_off + 256 + t * 128;
   const float qk = p.qk_scale;
-  const bool ragged = (p.N % kBlockN) != 0;
+  const bool ragged = (p.Nk % kBlockN) != 0;
   // this warpgroup's barriers, selected once (no run-time array indexing)
   const uint32_t bar_s_full = t ? sy.s_full[1] : sy.s_full[0];
   const uint32_t bar_p_ready = t ? sy.p_ready[1] : sy.p_ready[0];
@@ -709,10 +711,10 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       tmem_ld128_wait(tS, s);
 
       // Mask the diagonal tile (causal) and the ragged last tile: a key is
-      // kept iff key <= min(row, N-1) (causal) or key <= N-1.
+      // kept iff key <= min(row, Nk-1) (causal) or key <= Nk-1.
       const bool need_mask = (CAUSAL && j == n - 1) || (ragged && j == p.n_key_tiles - 1);
       if (need_mask) {
-        const int lim = (CAUSAL ? min(row, p.N - 1) : p.N - 1) - j * kBlockN;
+        const int lim = (CAUSAL ? min(row, p.Nk - 1) : p.Nk - 1) - j * kBlockN;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c > lim) s[c] = __float_as_uint(-INFINITY);
@@ -854,8 +856,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     const float lse_row = (m_ref + log2f(l)) * 0.69314718055994531f;
     if (ch.slot < 0) {
       // the chunk is the whole item: final O in bf16 and LSE, rows < N only
-      const bool store = row < p.N;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.N + (store ? row : 0)) * D;
+      const bool store = row < p.Nq;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Nq + (store ? row : 0)) * D;
       // rows are D * 2 bytes (a multiple of 32), so every row is 32-byte
       // aligned when O is; the API promises only 16
       const bool wide = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
@@ -881,7 +883,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
           }
         }
       }
-      if (store) p.lse[static_cast<size_t>(bh) * p.N + row] = lse_row;
+      if (store) p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse_row;
     } else {
       // a part of the item: merged once every part is in (merge_item)
       const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, inv_l, lse_row, false, p);
@@ -905,7 +907,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     for (int q = 0; q < kMaxPartsPerItem; ++q) ps.slot[q] = q < ps.n ? p.merge_slots[first + q] : -1;
     tc_fence_after_sync();
     merge_rows<D>(pm, ps, t, quad, tO, p.counters + pm.k * kCountersPerItem + t * 4 + quad, p.o, p.lse, p.part_o,
-                  p.part_lse, p.N);
+                  p.part_lse, p.Nq);
   }
 }
 

@@ -32,7 +32,8 @@ _I = ctypes.c_int
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
-    "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _P, _P]),
+    "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _P, _P]),
+    "fa_fwd_rect": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
@@ -138,6 +139,42 @@ def _call(entry, q, k, v, o, lse, causal, scale, stream) -> None:
         raise FAError(rc)
 
 
+def fa_fwd_rect(q, k, v, o, lse, causal: bool = False, scale: float | None = None,
+                stream=None) -> None:
+    """O and LSE for Nq query rows over Nk keys (top-left causal mask).
+
+    q, o: bf16 [B, H, Nq, d]; k, v: bf16 [B, H, Nk, d]; lse: fp32 [B, H, Nq].
+    """
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d] and k [B, H, Nk, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    _check("q", q, torch.bfloat16, (B, H, Nq, d), dev)
+    _check("k", k, torch.bfloat16, (B, H, Nk, d), dev)
+    _check("v", v, torch.bfloat16, (B, H, Nk, d), dev)
+    _check("o", o, torch.bfloat16, (B, H, Nq, d), dev)
+    _check("lse", lse, torch.float32, (B, H, Nq), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        rc = lib().fa_fwd_rect(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr(), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
+                               _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
+
+
+def attention_rect(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocating form of fa_fwd_rect: returns (O, LSE)."""
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_fwd_rect(q, k, v, o, lse, causal=causal, scale=scale, stream=stream)
+    return o, lse
+
+
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
     """Allocates O (bf16) and LSE (fp32) next to q and runs the forward; returns (O, LSE)."""
     o = torch.empty_like(q)
@@ -178,13 +215,16 @@ def attention_host(q, k, v, causal: bool = False, scale: float | None = None, de
     return oh, lseh
 
 
-def plan(B: int, H: int, N: int, d: int, causal: bool = False) -> tuple[int, int]:
+def plan(B: int, H: int, N: int, d: int, causal: bool = False,
+         n_keys: int | None = None) -> tuple[int, int]:
     """(attention grid, split items) that fa_fwd uses for these sizes on the current device.
 
-    Split items are computed in parts and merged inside the same launch.
+    N query rows and ``n_keys`` keys (default N, as fa_fwd).  Split items are
+    computed in parts and merged inside the same launch.
     """
     grid, nsplit = ctypes.c_int(0), ctypes.c_int(0)
-    rc = lib().fa_fwd_plan(int(B), int(H), int(N), int(d), int(bool(causal)),
+    nk = N if n_keys is None else n_keys
+    rc = lib().fa_fwd_plan(int(B), int(H), int(N), int(nk), int(d), int(bool(causal)),
                            ctypes.addressof(grid), ctypes.addressof(nsplit))
     if rc != FA_OK:
         raise FAError(rc)

@@ -66,9 +66,10 @@ enum fa_status {
  *   stream  : cudaStream_t as void*.
  *
  * Work division.  A work item is 256 query rows of one (b, h); its cost is
- * the key tiles of 128 its longer half visits.  With more items than SMs,
+ * the key tiles of 128 its longer half visits.  With more items than SMs
+ * (or fewer, but with at least 16 key tiles per SM to share out),
  * the concatenated steps of all items are cut into one equal contiguous
- * range per SM; an item cut between two CTAs is computed in parts, each
+ * range per CTA (at most one CTA per SM); an item cut between two CTAs is computed in parts, each
  * writing O normalised over its own keys and its logsumexp to the stream's
  * workspace; the CTA whose arrival completes an item's parts merges them
  * (O = sum_r exp(L_r - L) O_r, L = ln sum_r exp(L_r)) after its own work, so
@@ -82,6 +83,26 @@ enum fa_status {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * fa_fwd_rect — fa_fwd with Nq query rows and Nk keys per (b, h), which may
+ * differ.
+ *
+ *   q, o    : bf16 [B][H][Nq][d], contiguous.
+ *   k, v    : bf16 [B][H][Nk][d], contiguous.
+ *   lse     : fp32 [B][H][Nq].
+ *   causal  : 1 = key j visible to query i iff j <= i (top-left, the
+ *             convention non-square causal attention is checked against in
+ *             "How to profile and optimise kernels", Round 4); every row
+ *             sees key 0, so no row is ever fully masked.
+ * Few query rows over many keys (the decode shape) is the case this opens:
+ * when there are no more work items than SMs, the keys of each item are
+ * split over several CTAs (at least 16 key tiles each) and the parts merged
+ * in the same launch, as for fa_fwd.  Errors as fa_fwd, with Nq and Nk
+ * each >= 1 and B*H*Nq*d, B*H*Nk*d < 2^31.
+ */
+int fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int Nq, int Nk, int d, int causal, float scale, void* stream);
 
 /*
  * fa_fwd_noalloc — fa_fwd (same arguments, kernels, work division and
@@ -121,14 +142,16 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
                    int B, int H, int N, int d, int causal, float scale, void* stream);
 
 /*
- * fa_fwd_plan — the work division fa_fwd would use on the current device for
- * these sizes (no pointer is needed and nothing is launched or allocated):
+ * fa_fwd_plan — the work division fa_fwd_rect (fa_fwd: Nq = Nk = N) would use
+ * on the current device for these sizes (no pointer is needed and nothing
+ * is launched or allocated):
  * *num_ctas = the attention kernel's grid, *num_split_items = items computed
  * in parts (merged inside the same launch).  The paper has no counterpart;
  * it exists so that callers can see how the work is divided.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
  * FA_ERR_INVALID_ARG (sizes as for fa_fwd), FA_ERR_DEVICE or FA_ERR_LAUNCH.
  */
-int fa_fwd_plan(int B, int H, int N, int d, int causal, int* num_ctas, int* num_split_items);
+int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
+                int* num_split_items);
 
 /* Human-readable name of a status code; never NULL, static storage. */
 const char* fa_strerror(int code);

@@ -28,8 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_get_device_status",
-                     "fa_strerror", "fa_version", "fa_watchdog_selftest"]
+    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
+                     "fa_get_device_status", "fa_strerror", "fa_version", "fa_watchdog_selftest"]
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -86,9 +86,11 @@ def test_aliasing_outputs(fa):
     assert fa.fa_fwd_raw(Q, K, V, K + nbytes - 16, L, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
     assert fa.fa_fwd_raw(Q, K, V, O, V + 64, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
     assert fa.fa_fwd_raw(Q, K, V, O, O + nbytes - 4, 1, 2, 256, 64, 0, 0.125) == fa.FA_ERR_ALIAS
-    # touching but not overlapping is fine for the host checks (then no device here)
-    rc = fa.fa_fwd_raw(Q, K, V, Q + nbytes, L, 1, 2, 256, 64, 0, 0.125)
-    assert rc != fa.FA_ERR_ALIAS
+    # touching but not overlapping is fine for the host checks; the call then
+    # goes on to the device, so only where there is none (fake pointers)
+    if not torch.cuda.is_available():
+        rc = fa.fa_fwd_raw(Q, K, V, Q + nbytes, L, 1, 2, 256, 64, 0, 0.125)
+        assert rc != fa.FA_ERR_ALIAS
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
@@ -116,10 +118,11 @@ def test_plan_query_checks_its_arguments(fa):
 
     a, b = ctypes.c_int(0), ctypes.c_int(0)
     pa, pb = ctypes.addressof(a), ctypes.addressof(b)
-    assert fa.lib().fa_fwd_plan(1, 32, 4096, 128, 0, None, pb) == fa.FA_ERR_NULL
-    assert fa.lib().fa_fwd_plan(1, 32, 4096, 128, 0, pa, None) == fa.FA_ERR_NULL
-    for args in ((0, 1, 128, 64, 0), (1, 1, 0, 64, 0), (1, 1, 128, 96, 0), (1, 1, 128, 64, 2),
-                 (1 << 12, 1 << 12, 1 << 12, 128, 0)):
+    assert fa.lib().fa_fwd_plan(1, 32, 4096, 4096, 128, 0, None, pb) == fa.FA_ERR_NULL
+    assert fa.lib().fa_fwd_plan(1, 32, 4096, 4096, 128, 0, pa, None) == fa.FA_ERR_NULL
+    for args in ((0, 1, 128, 128, 64, 0), (1, 1, 0, 128, 64, 0), (1, 1, 128, 0, 64, 0),
+                 (1, 1, 128, 128, 96, 0), (1, 1, 128, 128, 64, 2),
+                 (1 << 12, 1 << 12, 1 << 12, 1, 128, 0), (1, 1, 1, 1 << 30, 128, 0)):
         assert fa.lib().fa_fwd_plan(*args, pa, pb) == fa.FA_ERR_INVALID_ARG
 
 
@@ -153,3 +156,19 @@ def test_noalloc_scratch_size_is_stated_in_the_header():
     ctas = int(_re.search(r"#define FA_NOALLOC_MAX_CTAS (\d+)", text).group(1))
     assert ctas == 160
     assert "42,278,912 bytes" in text and (ctas * 2 * 256 * 129 + 2048) * 4 == 42278912
+
+
+def test_rect_entry_checks_arguments(fa):
+    raw = fa.lib().fa_fwd_rect
+    # q, o: [1][2][64][64]; k, v: [1][2][512][64] -- sizes in bytes
+    qb, kb = 1 * 2 * 64 * 64 * 2, 1 * 2 * 512 * 64 * 2
+    assert raw(Q, K, V, O, L, 1, 2, 0, 512, 64, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert raw(Q, K, V, O, L, 1, 2, 64, 0, 64, 0, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert raw(Q, None, V, O, L, 1, 2, 64, 512, 64, 0, 0.125, None) == fa.FA_ERR_NULL
+    assert raw(Q, K + 8, V, O, L, 1, 2, 64, 512, 64, 0, 0.125, None) == fa.FA_ERR_ALIGN
+    # o overlapping the tail of k counts with k's own (longer) extent
+    assert raw(Q, K, V, K + kb - 16, L, 1, 2, 64, 512, 64, 0, 0.125, None) == fa.FA_ERR_ALIAS
+    assert raw(Q, K, V, Q + qb - 16, L, 1, 2, 64, 512, 64, 0, 0.125, None) == fa.FA_ERR_ALIAS
+    if not torch.cuda.is_available():  # past the host checks the call reaches the device
+        rc = raw(Q, K, V, Q + qb, L, 1, 2, 64, 512, 64, 0, 0.125, None)  # just past q: no alias
+        assert rc != fa.FA_ERR_ALIAS
