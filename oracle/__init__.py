@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the exact attention forward (test infrastructure only).
+"""fp64 CPU oracle for exact attention, forward and backward (test infrastructure only).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
 reference legs use this package.  It shares no code with the CUDA library.
@@ -12,4 +12,9 @@ from .attention import (  # noqa: F401
     online_max_sum,
     softmax_safe,
     tiled_attention,
+)
+from .attention_backward import (  # noqa: F401
+    attention_backward,
+    rowdot,
+    tiled_attention_backward,
 )
