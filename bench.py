@@ -30,7 +30,7 @@ import torch  # noqa: E402
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from exact_attention_20_gb300.inputs import HEADLINE, WORKLOADS, make_qkv  # noqa: E402
+from exact_attention_20_gb300.inputs import HEADLINE, WORKLOADS, make_grad, make_qkv  # noqa: E402
 
 METRIC = "attn fwd TFLOP/s (bf16, causal/non-causal) N=4096 d=128; % of GB300 BF16 peak"
 KERNEL_SOURCES = [
@@ -420,6 +420,68 @@ def run_decode(args):
         "clocks": clocks}), flush=True)
 
 
+def run_backward(args):
+    """dQ, dK, dV of the workload through fa_bwd, both masks, L2 flushed before every call.
+
+    One fa_bwd call is three launches (prep: D, L and the zeroed dQ
+    accumulator; the fused backward kernel; the dQ conversion), all inside
+    the timed span.  The algorithmic FLOPs are the backward's five products
+    (S, dP, dV, dK, dQ), 10 B H N^2 d non-causal and half that causal.
+    """
+    from exact_attention_20_gb300 import build as fa_build
+
+    fa_build.build()
+    from exact_attention_20_gb300 import fa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak, _, peak_src = measured_peaks()
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, seed=0, values=w.values, device=dev)
+    do = make_grad(w.B, w.H, w.N, w.d, seed=1, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sampler = ClockSampler(0)
+    sampler.start()
+    per_mask = {}
+    for causal in w.causal:
+        o, lse = fa.attention(q, k, v, causal=causal, scale=w.scale)
+        for _ in range(args.warmup):
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, scale=w.scale)
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        sampler.mark("t0")
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, scale=w.scale)
+            e1.record()
+        torch.cuda.synchronize(dev)
+        sampler.mark("t1")
+        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        f = 2.5 * flops(w, causal)
+        per_mask["causal" if causal else "non-causal"] = {
+            "ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "frac_of_measured_peak": f / (ms * 1e-3) / 1e12 / peak}
+    clocks = sampler.stop()
+    total_f = sum(2.5 * flops(w, c) for c in w.causal)
+    total_ms = sum(m["ms"] for m in per_mask.values())
+    value = total_f / (total_ms * 1e-3) / 1e12
+    dom = max(per_mask, key=lambda m: per_mask[m]["ms"])
+    print(json.dumps({
+        "metric": "attn bwd TFLOP/s (bf16, dQ dK dV, causal/non-causal); % of GB300 BF16 peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "masks": list(per_mask),
+                   "l2": "flushed before every call (256 MiB write, outside the events)"},
+        "per_mask": per_mask,
+        "roofline": {"bound": "tensor", "achieved": per_mask[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
+                     "frac": per_mask[dom]["frac_of_measured_peak"], "peak_kind": f"{peak_src} bf16 dense, burst",
+                     "timed_span": "one fa_bwd call: prep, fa_bwd_kernel, dQ conversion", "mask": dom},
+        "gpu_launches": args.steps * len(per_mask) * fa.BWD_KERNELS_PER_CALL,
+        "clocks": clocks}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,6 +494,8 @@ def main():
     ap.add_argument("--decode", action="store_true",
                     help="the few-query-rows shapes through fa_fwd_rect (HBM-bound), "
                          "instead of the headline step")
+    ap.add_argument("--backward", action="store_true",
+                    help="dQ, dK, dV of the workload through fa_bwd instead of the forward step")
     ap.add_argument("--quick", action="store_true",
                     help="only the timed kernel steps (for profiler runs): no clock sampling, "
                          "no end-to-end leg, no CPU baseline, no one-second warm-up floor")
@@ -442,6 +506,8 @@ def main():
         run_reference(args)
     elif args.decode:
         run_decode(args)
+    elif args.backward:
+        run_backward(args)
     else:
         run_ours(args)
 

@@ -17,7 +17,7 @@
 namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+using fa_internal::kWaitLimitNs;  // 2 s per pipeline wait
 constexpr int kMaxDevices = 64;
 
 __device__ int g_status;  // first failing wait site, 0 when healthy
@@ -321,6 +321,16 @@ namespace fa_internal {
 int check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    int B, int H, int N, int d, int causal, float scale) {
   return check_args(q, k, v, o, lse, B, H, N, N, d, causal, scale);
+}
+
+bool current_device(DeviceView* out) {
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (di == nullptr) return false;
+  out->status = di->status;
+  out->supported = di->supported;
+  out->num_sms = di->num_sms;
+  return true;
 }
 
 int fwd_with_scratch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

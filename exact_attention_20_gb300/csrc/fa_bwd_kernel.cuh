@@ -1,0 +1,678 @@
+// Exact attention backward for sm_103a: dQ, dK and dV from Q, K, V, the
+// forward's O and logsumexp L, and the upstream gradient dO.
+//
+// The method ("FlashAttention and kernels.", section "The backward pass:
+// recompute instead of remember"; "FlashAttention 2 from PyTorch to Triton",
+// section "What I am building"): the forward never stores P; every tile of it
+// is rebuilt from the scores and L as P = exp(S - L), with no running
+// maximum.  With D = rowsum(dO * O), one number per query row computed once,
+//   dV += P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//   dQ += scale dS K,  dK += scale dS^T Q.
+// Exponentials are taken in base 2: L is passed in log2 units and the scale
+// is folded into one FMA (the forward's exp2 trick, "How to profile and
+// optimise kernels", Round 4).
+//
+// GB300 mapping.  One CTA per (batch*head, block of 128 keys).  It keeps the
+// block's K and V in shared memory and its dK and dV accumulators in tensor
+// memory for the whole launch, and walks the query rows 64 at a time (a
+// step).  Every product is taken transposed so that the 128 keys are the
+// tensor-memory lanes and one thread owns one key row:
+//   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d
+//   dP^T = V dO^T     same shape
+//   dV  += P^T dO     M = 128 keys, N = d, K = 64 queries (P^T read from TMEM)
+//   dK  += dS^T Q     same shape (dS^T read from shared memory)
+//   dQ^T = K^T dS^T   M = d (128 lanes), N = 64 queries, K = 128 keys
+// Every key block adds to every query row's dQ, so each step's dQ^T is added
+// into an fp32 accumulator in global memory by TMA reductions (the adds are
+// done by the memory system, not by atomics from threads).  With d = 64 the
+// dQ^T product still has M = 128: rows 64-127 of its A operand are V^T (the
+// tile that follows K in shared memory) and those lanes are ignored.
+//
+// Warp roles (12 warps, 384 threads):
+//   warp 0     TMA producer: K and V once; Q, dO and their rows' L and D per step
+//   warp 1     MMA issuer (one lane issues), owner of the TMEM allocation
+//   warps 2-3  idle
+//   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
+//   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread
+// Tensor memory (fp32 columns): S^T in two buffers at 0 and 64, dP^T at 128,
+// dQ^T at 192, dV at 256, dK at 384.  P^T (bf16, two per column) overwrites
+// the first 32 columns of its S^T buffer.  S^T has two buffers so that the
+// next step's S^T is computed while this step's P^T still feeds dV.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kBlockK = 128;   // keys per CTA
+constexpr int kBlockQ = 64;    // query rows per step
+constexpr int kThreads = 384;
+constexpr int kStages = 2;     // Q / dO ring depth
+constexpr int kLoadWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kDsWarp0 = 4;    // first warp of the P / dS warpgroup
+constexpr int kDrainWarp0 = 8; // first warp of the dQ drain warpgroup
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;    // + 64 * buffer
+constexpr uint32_t kColDP = 128;
+constexpr uint32_t kColDQ = 192;
+constexpr uint32_t kColDV = 256;
+constexpr uint32_t kColDK = 384;
+
+// Codes recorded in the device status word when a wait gives up.
+constexpr int kSiteProducer = 11;
+constexpr int kSiteMma = 12;
+constexpr int kSiteDs = 13;
+constexpr int kSiteDrain = 14;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+  static constexpr int kKSlab = kBlockK * 128;  // 128 rows x 64 bf16 (one TMA box)
+  static constexpr int kQSlab = kBlockQ * 128;  // 64 rows x 64 bf16
+  static constexpr int kKTile = (D / 64) * kKSlab;
+  static constexpr int kQTile = (D / 64) * kQSlab;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKTile;  // directly after K (see the d = 64 note above)
+  static constexpr int kStageOff = kVOff + kKTile;
+  static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
+  static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries]
+  static constexpr int kDqOff = kDsOff + 2 * kDsBytes;
+  static constexpr int kDqWarpBytes = kBlockQ * 32 * 4;   // one drain warp: [64 rows][32 d] fp32
+  static constexpr int kDqBytes = (D / 32) * kDqWarpBytes;
+  static constexpr int kLdOff = kDqOff + kDqBytes;        // per stage: L[64] then D[64], fp32
+  static constexpr int kLdBytes = 2 * kBlockQ * 4;
+  static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
+  static constexpr int kNumBars = 16;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStageBytes % 1024 == 0,
+                "operand tiles must sit on 1024-byte swizzle atoms");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+struct BwdParams {
+  __nv_bfloat16* dk;      // [BH][Nk][D]
+  __nv_bfloat16* dv;      // [BH][Nk][D]
+  const float* lp;        // workspace [BH][Nq_pad]: L * log2(e); +inf on padding rows
+  const float* dsum;      // workspace [BH][Nq_pad]: rowsum(dO * O); 0 on padding rows
+  int* status;            // device status word (0 = ok)
+  int Nq, Nk, Nq_pad;     // query rows, keys, query rows rounded up to 64
+  int n_qt;               // ceil(Nq / 64)
+  float qk_scale;         // scale * log2(e)
+  float scale;
+  unsigned long long wait_limit_ns;
+};
+
+// Barrier addresses.  The pairs (one per stage or buffer) are adjacent, so
+// buffer b's barrier is the pair's address + 8 b (no run-time array index,
+// which would put the struct in local memory).
+struct Sync {
+  uint32_t kv_full, stage_full0, stage_empty0, s_full0, dp_full, sm_done, dq_full, dq_free, ds_free0,
+      acc_done;
+  volatile int* abort_flag;
+  __device__ __forceinline__ uint32_t stage_full(int b) const { return stage_full0 + 8 * b; }
+  __device__ __forceinline__ uint32_t stage_empty(int b) const { return stage_empty0 + 8 * b; }
+  __device__ __forceinline__ uint32_t s_full(int b) const { return s_full0 + 8 * b; }
+  __device__ __forceinline__ uint32_t ds_free(int b) const { return ds_free0 + 8 * b; }
+};
+
+// Bounded wait: true when the phase completed; false if this CTA is aborting
+// or the wait ran past the limit (then the failure is recorded).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Sync& sy,
+                                           const BwdParams& p, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t polls = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++polls & 31u) == 0u) {
+      if (*sy.abort_flag) return false;
+      if (global_timer_ns() - t0 > p.wait_limit_ns) {
+        *sy.abort_flag = 1;
+        atomicCAS(p.status, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+// 3-D tiled reduction into global memory: tensor[...] += the shared-memory
+// box at `src` (element type and box from the tensor map); elements outside
+// the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                                  int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA producer (one thread)
+// ---------------------------------------------------------------------------
+// K and V are read once per CTA (evict first); the Q and dO tiles of a head
+// are read by all of its key blocks, so they are kept in L2 (evict last).
+template <int D>
+__device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                                             const CUtensorMap* tmV, const CUtensorMap* tmDO,
+                                             uint32_t sbase, const Sync& sy, const BwdParams& p,
+                                             int bh, int kb, int j0, int n) {
+  using C = Cfg<D>;
+  const uint64_t pol_kv = l2_policy_evict_first();
+  const uint64_t pol_q = l2_policy_evict_last();
+  mbar_arrive_expect_tx(sy.kv_full, 2 * C::kKTile);
+#pragma unroll
+  for (int s = 0; s < D / 64; ++s) {
+    tma_load_3d_hint(sbase + C::kKOff + s * C::kKSlab, tmK, sy.kv_full, s * 64, kb * kBlockK, bh, pol_kv);
+    tma_load_3d_hint(sbase + C::kVOff + s * C::kKSlab, tmV, sy.kv_full, s * 64, kb * kBlockK, bh, pol_kv);
+  }
+  int it = 0;
+  for (; it < n; ++it) {
+    const int st = it & 1;
+    if (!wait_phase(sy.stage_empty(st), ((it >> 1) & 1) ^ 1, sy, p, kSiteProducer)) break;
+    const int q0 = (j0 + it) * kBlockQ;
+    const uint32_t full = sy.stage_full(st);
+    mbar_arrive_expect_tx(full, C::kStageBytes + C::kLdBytes);
+    const uint32_t dst = sbase + C::kStageOff + st * C::kStageBytes;
+#pragma unroll
+    for (int s = 0; s < D / 64; ++s) {
+      tma_load_3d_hint(dst + s * C::kQSlab, tmQ, full, s * 64, q0, bh, pol_q);
+      tma_load_3d_hint(dst + C::kQTile + s * C::kQSlab, tmDO, full, s * 64, q0, bh, pol_q);
+    }
+    // L and D of the step's rows: 256 bytes each, 16-byte aligned because
+    // the workspace rows are padded to a multiple of 64
+    const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad + q0;
+    const uint32_t ld = sbase + C::kLdOff + st * C::kLdBytes;
+    bulk_load(ld, p.lp + row0, kBlockQ * 4, full);
+    bulk_load(ld + kBlockQ * 4, p.dsum + row0, kBlockQ * 4, full);
+  }
+  // Drain: every copy this thread started lands before the CTA exits.
+  mbar_wait_bounded(sy.kv_full, 0, p.wait_limit_ns);
+  for (int c = it > 2 ? it - 2 : 0; c < it; ++c)
+    mbar_wait_bounded(sy.stage_full(c & 1), (c >> 1) & 1, p.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one warp; lane 0 issues)
+// ---------------------------------------------------------------------------
+// Operand descriptors.  K and V tiles: 64-column slabs of 128 rows (16 KB);
+// Q and dO tiles: slabs of 64 rows (8 KB); dS^T: one slab of 128 rows.  All
+// 128-byte swizzled; 8-row groups are 1024 bytes apart (the stride byte
+// offset).  As a K-major operand a tile advances 32 bytes per 16 columns of
+// d inside a slab; as an MN-major operand it advances 2048 bytes per 16 rows
+// and its slabs (64 values of the N or M dimension each) are the leading
+// byte offset apart.
+// Stage and buffer b's descriptors are the first one's, moved by b times the
+// stage (or buffer) size.
+template <int D>
+struct Desc {
+  using C = Cfg<D>;
+  uint64_t k_kmaj, v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_kmaj0, ds_mn0;
+  __device__ __forceinline__ explicit Desc(uint32_t sbase) {
+    k_kmaj = sdesc_sw128(sbase + C::kKOff, 16, 1024);
+    v_kmaj = sdesc_sw128(sbase + C::kVOff, 16, 1024);
+    kt_mn = sdesc_sw128(sbase + C::kKOff, C::kKSlab, 1024);
+    const uint32_t st = sbase + C::kStageOff;
+    q_kmaj0 = sdesc_sw128(st, 16, 1024);
+    do_kmaj0 = sdesc_sw128(st + C::kQTile, 16, 1024);
+    q_mn0 = sdesc_sw128(st, C::kQSlab, 1024);
+    do_mn0 = sdesc_sw128(st + C::kQTile, C::kQSlab, 1024);
+    const uint32_t ds = sbase + C::kDsOff;
+    ds_kmaj0 = sdesc_sw128(ds, 16, 1024);
+    ds_mn0 = sdesc_sw128(ds, C::kDsBytes, 1024);  // N = 64: one slab, the leading offset is not used
+  }
+  __device__ __forceinline__ uint64_t q_kmaj(int b) const { return sdesc_advance(q_kmaj0, b * C::kStageBytes); }
+  __device__ __forceinline__ uint64_t do_kmaj(int b) const { return sdesc_advance(do_kmaj0, b * C::kStageBytes); }
+  __device__ __forceinline__ uint64_t q_mn(int b) const { return sdesc_advance(q_mn0, b * C::kStageBytes); }
+  __device__ __forceinline__ uint64_t do_mn(int b) const { return sdesc_advance(do_mn0, b * C::kStageBytes); }
+  __device__ __forceinline__ uint64_t ds_kmaj(int b) const { return sdesc_advance(ds_kmaj0, b * C::kDsBytes); }
+  __device__ __forceinline__ uint64_t ds_mn(int b) const { return sdesc_advance(ds_mn0, b * C::kDsBytes); }
+};
+
+// S^T = K Q^T or dP^T = V dO^T: A = the 128-key tile, B = the 64-row tile,
+// both K-major over d.
+template <int D>
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint64_t a, uint64_t b) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32_ab(kBlockK, kBlockQ, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    umma_ss(d_tmem, sdesc_advance(a, (kk / 4) * C::kKSlab + (kk % 4) * 32),
+            sdesc_advance(b, (kk / 4) * C::kQSlab + (kk % 4) * 32), idesc, kk > 0 ? 1u : 0u);
+}
+
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy,
+                                        const BwdParams& p, int n) {
+  const bool leader = (threadIdx.x & 31) == 0;
+  bool ok = true;
+  auto wait_voted = [&](uint32_t bar, uint32_t par) {
+    ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
+  };
+  const Desc<D> ds(sbase);
+  const uint32_t tm_dp = tmem + kColDP, tm_dq = tmem + kColDQ;
+  const uint32_t tm_dv = tmem + kColDV, tm_dk = tmem + kColDK;
+  constexpr uint32_t id_acc = idesc_bf16_f32_ab(kBlockK, D, false, true);      // dV, dK
+  constexpr uint32_t id_dq = idesc_bf16_f32_ab(128, kBlockQ, true, true);      // dQ^T
+  wait_voted(sy.kv_full, 0);
+  if (n > 0 && ok) {
+    wait_voted(sy.stage_full(0), 0);
+    if (ok) {
+      tc_fence_after_sync();
+      if (leader) {
+        issue_scores<D>(tmem + kColS, ds.k_kmaj, ds.q_kmaj(0));
+        umma_commit(sy.s_full(0));
+        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(0));
+        umma_commit(sy.dp_full);
+      }
+      __syncwarp();
+    }
+  }
+  for (int it = 0; it < n && ok; ++it) {
+    const int b = it & 1;
+    const bool more = it + 1 < n;
+    if (more) {
+      // S^T of the next step into the other buffer: its previous P^T fed the
+      // dV product of step it-1, issued before this one.
+      wait_voted(sy.stage_full(b ^ 1), ((it + 1) >> 1) & 1);
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_scores<D>(tmem + kColS + (b ^ 1) * 64, ds.k_kmaj, ds.q_kmaj(b ^ 1));
+        umma_commit(sy.s_full(b ^ 1));
+      }
+      __syncwarp();
+    }
+    wait_voted(sy.sm_done, it & 1);  // P^T in TMEM, dS^T in shared memory; S^T, dP^T read
+    if (!ok) break;
+    tc_fence_after_sync();
+    if (leader) {
+      if (more) {
+        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(b ^ 1));
+        umma_commit(sy.dp_full);
+      }
+      const uint32_t acc = it > 0 ? 1u : 0u;
+#pragma unroll
+      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dV += P^T dO
+        umma_ts(tm_dv, tmem + kColS + b * 64 + kk * 8, sdesc_advance(ds.do_mn(b), kk * 2048), id_acc,
+                kk > 0 ? 1u : acc);
+#pragma unroll
+      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
+        umma_ss(tm_dk, sdesc_advance(ds.ds_kmaj(b), kk * 32), sdesc_advance(ds.q_mn(b), kk * 2048), id_acc,
+                kk > 0 ? 1u : acc);
+    }
+    __syncwarp();
+    if (it > 0) wait_voted(sy.dq_free, (it - 1) & 1);  // the drain has read dQ^T of the last step
+    if (!ok) break;
+    tc_fence_after_sync();
+    if (leader) {
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T
+        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
+                kk > 0 ? 1u : 0u);
+      umma_commit(sy.dq_full);
+      umma_commit(sy.stage_empty(b));
+      umma_commit(sy.ds_free(b));
+    }
+    __syncwarp();
+  }
+  // Completes when every product issued above has: the epilogue's signal,
+  // and the condition for releasing tensor memory.
+  if (leader) umma_commit(sy.acc_done);
+  __syncwarp();
+  mbar_wait_bounded(sy.acc_done, 0, p.wait_limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// P and dS (warps 4-7, one key row per thread), then the dK, dV epilogue
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync& sy,
+                                       const BwdParams& p, int bh, int kb, int j0, int n) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quad = warp & 3;                 // TMEM lanes 32*quad .. 32*quad+31
+  const int r = quad * 32 + lane;            // key row within the block
+  const int key = kb * kBlockK + r;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint64_t qk2 = f2_pack(p.qk_scale, p.qk_scale);
+  bool ok = true;
+  for (int it = 0; it < n; ++it) {
+    const int b = it & 1;
+    const int q0 = (j0 + it) * kBlockQ;
+    bool w = wait_phase(sy.s_full(b), (it >> 1) & 1, sy, p, kSiteDs);
+    w = w && wait_phase(sy.stage_full(b), (it >> 1) & 1, sy, p, kSiteDs);  // L, D of the step
+    ok = __all_sync(0xffffffffu, w);
+    if (!ok) break;
+    tc_fence_after_sync();
+    const float* Lrow = reinterpret_cast<const float*>(smem + C::kLdOff + b * C::kLdBytes);
+    const float* Drow = Lrow + kBlockQ;
+    const uint32_t tS = tmem + lane_off + kColS + b * 64;
+
+    // P^T row: p_c = exp2(s_c * scale * log2 e - L_c * log2 e) for query q0 + c.
+    // Query rows past the end have L = +inf (p = 0).  Key `key` is visible to
+    // query q0 + c iff key < Nk and (not causal or key <= q0 + c).
+    float pf[kBlockQ];
+    {
+      uint32_t s[kBlockQ];
+      tmem_ld64_wait(tS, s);
+#pragma unroll
+      for (int c = 0; c < kBlockQ; c += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(Lrow + c);
+        const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2,
+                                    f2_pack(-l4.x, -l4.y));
+        const uint64_t x23 = f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), qk2,
+                                    f2_pack(-l4.z, -l4.w));
+        float a0, a1, a2, a3;
+        f2_unpack(x01, a0, a1);
+        f2_unpack(x23, a2, a3);
+        pf[c] = ex2_approx(a0);
+        pf[c + 1] = ex2_approx(a1);
+        pf[c + 2] = ex2_approx(a2);
+        pf[c + 3] = ex2_approx(a3);
+      }
+    }
+    const int cmin = key >= p.Nk ? kBlockQ : (CAUSAL ? key - q0 : 0);  // first visible column
+    if (cmin > 0) {
+#pragma unroll
+      for (int c = 0; c < kBlockQ; ++c) pf[c] = c < cmin ? 0.f : pf[c];
+    }
+    {
+      uint32_t pk[kBlockQ / 2];
+#pragma unroll
+      for (int i = 0; i < kBlockQ / 2; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
+      tmem_st32(tS, pk);
+    }
+
+    // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16 and written to the
+    // 128-byte-swizzled dS^T tile (16-byte chunk ch of row r at chunk ch ^ (r % 8)).
+    w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
+    if (it >= 2) w = w && wait_phase(sy.ds_free(b), ((it >> 1) - 1) & 1, sy, p, kSiteDs);
+    ok = __all_sync(0xffffffffu, w);
+    if (!ok) break;
+    tc_fence_after_sync();
+    uint8_t* ds_row = smem + C::kDsOff + b * C::kDsBytes + r * 128;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t d32[32];
+      tmem_ld32_wait(tmem + lane_off + kColDP + h * 32, d32);
+      uint32_t wds[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = h * 32 + 2 * i;
+        const float2 dd = *reinterpret_cast<const float2*>(Drow + c);
+        const float g0 = pf[c] * (__uint_as_float(d32[2 * i]) - dd.x);
+        const float g1 = pf[c + 1] * (__uint_as_float(d32[2 * i + 1]) - dd.y);
+        wds[i] = pack_bf16x2(g0, g1);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ch = h * 4 + q;
+        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) * 16)) =
+            make_uint4(wds[4 * q], wds[4 * q + 1], wds[4 * q + 2], wds[4 * q + 3]);
+      }
+    }
+    tmem_st_wait();            // P^T is in tensor memory
+    fence_proxy_async_smem();  // dS^T is visible to the tensor core
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sy.sm_done);
+  }
+
+  // Epilogue: dV and scale * dK of this thread's key row, bf16.  A block with
+  // no visible query row (causal, keys past the last query) writes zeros.
+  bool w = wait_phase(sy.acc_done, 0, sy, p, kSiteDs);
+  ok = __all_sync(0xffffffffu, ok && w);
+  if (!ok || *sy.abort_flag) return;
+  tc_fence_after_sync();
+  const bool store = key < p.Nk;
+  const size_t row_off = (static_cast<size_t>(bh) * p.Nk + key) * D;
+#pragma unroll 1
+  for (int which = 0; which < 2; ++which) {
+    __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row_off;
+    const float mul = which == 0 ? 1.f : p.scale;
+    const uint32_t col = which == 0 ? kColDV : kColDK;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t a[32];
+      if (n > 0) {
+        tmem_ld32_wait(tmem + lane_off + col + c0, a);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+      if (store) {
+        uint4* out = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) out[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ drain (warps 8-11): thread = one row of dQ^T (one column of d)
+// ---------------------------------------------------------------------------
+// Each warp owns 32 columns of d.  Per step it moves its [64 queries][32]
+// block of dQ^T from tensor memory into its own staging area (row-major, so
+// a warp's store covers 128 contiguous bytes) and adds it into the fp32 dQ
+// accumulator with one TMA reduction; rows past the last query are outside
+// the tensor map and skipped.  With d = 64 only warps 8 and 9 hold dQ^T rows.
+template <int D>
+__device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t sbase, uint32_t tmem,
+                                          const CUtensorMap* tmDq, const Sync& sy, const BwdParams& p,
+                                          int bh, int j0, int n) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const bool has_rows = quad * 32 < D;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  float* stage = reinterpret_cast<float*>(smem + C::kDqOff + (has_rows ? quad : 0) * C::kDqWarpBytes);
+  const uint32_t stage_s = sbase + C::kDqOff + (has_rows ? quad : 0) * C::kDqWarpBytes;
+  bool issued = false;
+  for (int it = 0; it < n; ++it) {
+    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full, it & 1, sy, p, kSiteDrain));
+    if (!ok) break;
+    tc_fence_after_sync();
+    uint32_t x[kBlockQ];
+    tmem_ld64_wait(tmem + lane_off + kColDQ, x);
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sy.dq_free);
+    if (!has_rows) continue;
+    if (lane == 0 && issued) tma_store_wait_read0();  // the last reduction has read the staging area
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < kBlockQ; ++q) stage[q * 32 + lane] = __uint_as_float(x[q]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_3d(tmDq, stage_s, quad * 32, (j0 + it) * kBlockQ, bh);
+      tma_store_commit();
+      issued = true;
+    }
+    __syncwarp();
+  }
+  if (lane == 0 && issued) tma_store_wait_all0();
+}
+
+// ---------------------------------------------------------------------------
+// Kernel: grid (B*H, key blocks); key block 0 (the longest under the causal
+// mask) of every head is scheduled first
+// ---------------------------------------------------------------------------
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmDq, const BwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int kb = blockIdx.y;
+  // Query steps of this key block: under the top-left causal mask key j is
+  // seen by queries i >= j, so the first step is the one holding query kb*128.
+  const int j0 = CAUSAL ? (kb * kBlockK) / kBlockQ : 0;
+  const int n = p.n_qt > j0 ? p.n_qt - j0 : 0;
+
+  Sync sy;
+  {
+    uint32_t b = sbase + C::kBarOff;
+    auto next = [&]() { const uint32_t r = b; b += 8; return r; };
+    sy.kv_full = next();
+    sy.stage_full0 = next();
+    next();
+    sy.stage_empty0 = next();
+    next();
+    sy.s_full0 = next();
+    next();
+    sy.dp_full = next();
+    sy.sm_done = next();
+    sy.dq_full = next();
+    sy.dq_free = next();
+    sy.ds_free0 = next();
+    next();
+    sy.acc_done = next();
+  }
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
+  sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+
+  if (threadIdx.x == 0) {
+    mbar_init(sy.kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sy.stage_full(i), 1);
+      mbar_init(sy.stage_empty(i), 1);
+      mbar_init(sy.s_full(i), 1);
+      mbar_init(sy.ds_free(i), 1);
+    }
+    mbar_init(sy.dp_full, 1);
+    mbar_init(sy.sm_done, 4);  // one arrival per P / dS warp
+    mbar_init(sy.dq_full, 1);
+    mbar_init(sy.dq_free, 4);  // one arrival per drain warp
+    mbar_init(sy.acc_done, 1);
+    *sy.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmDO);
+  }
+  if (warp == kDrainWarp0 && lane == 0) tma_prefetch_desc(&tmDq);
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kLoadWarp) {
+    if (lane == 0) run_producer<D>(&tmQ, &tmK, &tmV, &tmDO, sbase, sy, p, bh, kb, j0, n);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    run_mma<D, CAUSAL>(sbase, tmem, sy, p, n);
+  } else if (warp >= kDsWarp0 && warp < kDsWarp0 + 4) {
+    run_ds<D, CAUSAL>(smem, tmem, sy, p, bh, kb, j0, n);
+  } else if (warp >= kDrainWarp0) {
+    run_drain<D>(smem, sbase, tmem, &tmDq, sy, p, bh, j0, n);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Before: D = rowsum(dO * O) and L in log2 units per query row (padded to a
+// multiple of 64 rows per head: L = +inf, D = 0), and the dQ accumulator
+// zeroed.  One warp per row; the products of two bf16 values are exact in
+// fp32 and summed in fp32.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                   const float* __restrict__ lse, float* __restrict__ lp, float* __restrict__ dsum,
+                   float* __restrict__ dq_acc, int BH, int Nq, int Nq_pad) {
+  constexpr int kPer = D / 32;  // elements per lane
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const long long rows = static_cast<long long>(BH) * Nq_pad;
+  for (long long row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += warps) {
+    const int bh = static_cast<int>(row / Nq_pad);
+    const int i = static_cast<int>(row % Nq_pad);
+    float dot = 0.f;
+    if (i < Nq) {
+      const size_t base = (static_cast<size_t>(bh) * Nq + i) * D + lane * kPer;
+      __nv_bfloat162 ov[kPer / 2], gv[kPer / 2];
+      if constexpr (kPer == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+        const uint2 g = *reinterpret_cast<const uint2*>(dout + base);
+        ov[0] = *reinterpret_cast<const __nv_bfloat162*>(&a.x);
+        ov[1] = *reinterpret_cast<const __nv_bfloat162*>(&a.y);
+        gv[0] = *reinterpret_cast<const __nv_bfloat162*>(&g.x);
+        gv[1] = *reinterpret_cast<const __nv_bfloat162*>(&g.y);
+      } else {
+        ov[0] = *reinterpret_cast<const __nv_bfloat162*>(o + base);
+        gv[0] = *reinterpret_cast<const __nv_bfloat162*>(dout + base);
+      }
+#pragma unroll
+      for (int e = 0; e < kPer / 2; ++e) {
+        const float2 a = __bfloat1622float2(ov[e]);
+        const float2 g = __bfloat1622float2(gv[e]);
+        dot = fmaf(a.x, g.x, dot);
+        dot = fmaf(a.y, g.y, dot);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      float* acc = dq_acc + (static_cast<size_t>(bh) * Nq + i) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        *reinterpret_cast<float4*>(acc) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        *reinterpret_cast<float2*>(acc) = make_float2(0.f, 0.f);
+      }
+    }
+    if (lane == 0) {
+      lp[row] = i < Nq ? lse[static_cast<size_t>(bh) * Nq + i] * 1.4426950408889634f : INFINITY;
+      dsum[row] = i < Nq ? dot : 0.f;
+    }
+  }
+}
+
+// After: dQ = bf16(scale * accumulator), eight values per thread.
+__global__ void __launch_bounds__(256)
+fa_bwd_dq_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long long n8,
+                 float scale) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(dq)[i] =
+        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                   pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+  }
+}
+
+}  // namespace bwd
+}  // namespace fa

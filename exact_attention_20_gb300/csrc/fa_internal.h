@@ -22,4 +22,17 @@ int check_fwd_args(const void* q, const void* k, const void* v, const void* o, c
 int fwd_with_scratch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                      int N, int d, int causal, float scale, void* stream, const Scratch& scratch);
 
+// The current device as the library sees it: its status word (written by a
+// kernel whose bounded wait gave up), whether it is an sm_103 part, and its
+// SM count.  False when a CUDA call failed.
+struct DeviceView {
+  int* status = nullptr;
+  bool supported = false;
+  int num_sms = 0;
+};
+bool current_device(DeviceView* out);
+
+// Wait limit of every pipeline wait inside the kernels, in nanoseconds.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
 }  // namespace fa_internal

@@ -141,6 +141,31 @@ __device__ __forceinline__ void tma_store_wait_all0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Bulk copy (no tensor map) of `bytes` from global to this CTA's shared
+// memory, counted against `bar`'s transaction bytes.  Both addresses 16-byte
+// aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// dst[i] += src[i] for bytes / 4 fp32 values, shared -> global, done by the
+// memory system (a bulk async-group operation: commit and wait with the
+// bulk-group calls above).  Both addresses 16-byte aligned, `bytes` a
+// multiple of 16.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
+// Barrier `id` (1-15) over `count` threads, a multiple of 32.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ---------------------------------------------------------------------------
@@ -214,6 +239,12 @@ __device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes)
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) |
          ((M >> 4) << 24);
+}
+
+// The same with A's major-ness as well, in bit 15 (0 = K-major, 1 = MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(uint32_t M, uint32_t N, bool a_mn_major,
+                                                         bool b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T ; issued by one thread.

@@ -1,6 +1,6 @@
 """Thin ctypes binding of libfa_gb300.so: argument marshalling only.
 
-Every step of the attention forward runs in the CUDA library; this module
+Every step of the attention forward and backward runs in the CUDA library; this module
 checks tensor metadata, passes raw device pointers and sizes through the C
 ABI declared in include/fa_gb300.h, and turns status codes into exceptions.
 There is no CPU fallback: without the built library, or on a device other
@@ -34,6 +34,7 @@ SIGNATURES = {
     "fa_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _P, _P]),
     "fa_fwd_rect": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
@@ -175,6 +176,46 @@ def attention_rect(q, k, v, causal: bool = False, scale: float | None = None, st
     return o, lse
 
 
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal: bool = False, scale: float | None = None,
+           stream=None) -> None:
+    """dQ, dK, dV into caller-owned tensors, from the forward's O and LSE.
+
+    q, o, do, dq: bf16 [B, H, Nq, d]; k, v, dk, dv: bf16 [B, H, Nk, d];
+    lse: fp32 [B, H, Nq] (the forward's natural-log logsumexp).  Same mask
+    and scale as the forward that produced O and LSE.
+    """
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, H, Nq, d] and k [B, H, Nk, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for name, t in (("q", q), ("o", o), ("do", do), ("dq", dq)):
+        _check(name, t, torch.bfloat16, (B, H, Nq, d), dev)
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check(name, t, torch.bfloat16, (B, H, Nk, d), dev)
+    _check("lse", lse, torch.float32, (B, H, Nq), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        rc = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d,
+                          int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
+
+
+def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
+                       stream=None):
+    """Allocating form of fa_bwd: returns (dQ, dK, dV)."""
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, scale=scale, stream=stream)
+    return dq, dk, dv
+
+
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
     """Allocates O (bf16) and LSE (fp32) next to q and runs the forward; returns (O, LSE)."""
     o = torch.empty_like(q)
@@ -232,6 +273,7 @@ def plan(B: int, H: int, N: int, d: int, causal: bool = False,
 
 
 KERNELS_PER_CALL = 1  # every fa_fwd call is one kernel launch
+BWD_KERNELS_PER_CALL = 3  # fa_bwd: prep (D, L, zero dQ accumulator), the backward kernel, dQ conversion
 
 
 def device_status(stream=None) -> int:

@@ -1,6 +1,7 @@
 """Seeded synthetic inputs shared by the tests, the bench and the oracle checks.
 
-This module holds no attention arithmetic: it only draws Q, K, V.  The pages
+This module holds no attention arithmetic: it only draws Q, K, V (and the
+upstream gradient dO for the backward).  The pages
 measure on i.i.d. Gaussian tensors of shape (B, H, N, d) ("How to profile and
 optimise kernels", section "How I profile": three torch.randn tensors viewed
 as (B, H, N, D); the bench of "FlashAttention and kernels.", section "Build
@@ -71,6 +72,13 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int = 0, values: str = "norma
     elif values != "normal":
         raise ValueError(f"unknown value recipe {values!r}")
     return q.to(dtype).contiguous(), k.to(dtype).contiguous(), v.to(dtype).contiguous()
+
+
+def make_grad(B: int, H: int, N: int, d: int, seed: int = 0, device="cpu", dtype=torch.bfloat16):
+    """The upstream gradient dO for the backward: i.i.d. N(0, 1), [B, H, N, d], rounded to ``dtype``."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) + 7919)
+    return torch.randn((B, H, N, d), generator=g, device=device, dtype=torch.float32).to(dtype).contiguous()
 
 
 def make_workload(name: str, seed: int = 0, device="cpu"):

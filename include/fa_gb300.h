@@ -1,5 +1,6 @@
 /*
- * fa_gb300.h — C ABI of the GB300 (sm_103a) fused exact attention forward.
+ * fa_gb300.h — C ABI of the GB300 (sm_103a) fused exact attention forward
+ * and backward.
  *
  * The operation.  For every batch b, head h and query row i,
  *
@@ -154,6 +155,47 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
                 int* num_split_items);
 
 /* Human-readable name of a status code; never NULL, static storage. */
+/*
+ * fa_bwd — attention backward: the gradients of O = softmax(scale Q K^T [mask]) V
+ * with respect to Q, K and V, for an upstream gradient dO.
+ *
+ *   q, o, dout : bf16 [B][H][Nq][d], contiguous, read only (o is the forward's output).
+ *   k, v       : bf16 [B][H][Nk][d], contiguous, read only.
+ *   lse        : fp32 [B][H][Nq], the forward's natural-log logsumexp, read only.
+ *   dq         : bf16 [B][H][Nq][d]; written.
+ *   dk, dv     : bf16 [B][H][Nk][d]; written.  No output may overlap an input or another output.
+ *   B, H, Nq, Nk, d, causal, scale : as for fa_fwd_rect (the same values the
+ *             forward used; causal is the top-left mask), with
+ *             B*H*ceil(Nq/64)*64*d < 2^31, B*H*Nk*d < 2^31 and ceil(Nk/128) <= 65535.
+ *   stream     : cudaStream_t as void*.
+ *
+ * The method is the recompute-from-L backward of "FlashAttention and
+ * kernels." (gtadkapally.com, section "The backward pass: recompute instead
+ * of remember"): P = exp(scale Q K^T - L) rebuilt tile by tile, never stored;
+ * D = rowsum(dO * O) once per query row; dV = P^T dO, dP = dO V^T,
+ * dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.  P and dS are rounded
+ * to bf16 before their products; every product accumulates in fp32; the
+ * outputs are rounded once to bf16.  dQ sums the contributions of all key
+ * blocks in an fp32 accumulator in the order the blocks finish, so its last
+ * bit may differ between runs; dK and dV are deterministic.
+ *
+ * Three launches on `stream`: prep (D, L in log2 units, accumulator zeroed),
+ * the backward kernel (one CTA per (b, h, 128-key block)), and the dQ
+ * conversion.  Device memory: besides the status word, one workspace per
+ * stream of B*H*Nq*d*4 + 2*B*H*ceil(Nq/64)*64*4 bytes (rounded up to 256),
+ * allocated on the first call on that stream and grown (after synchronising
+ * the stream) when a call needs more; kept until the process exits.
+ *
+ * Returns FA_OK or a negative fa_status: FA_ERR_INVALID_ARG, FA_ERR_NULL,
+ * FA_ERR_ALIGN (a bf16 tensor not 16-byte aligned, lse not 4-byte aligned),
+ * FA_ERR_ALIAS, FA_ERR_DEVICE or FA_ERR_LAUNCH (also when the workspace
+ * cannot be allocated).  A kernel wait that gives up is reported by
+ * fa_get_device_status, as for the forward.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+           int causal, float scale, void* stream);
+
 const char* fa_strerror(int code);
 
 /*

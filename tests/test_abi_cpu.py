@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == ["fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
+    assert names == ["fa_bwd", "fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
                      "fa_get_device_status", "fa_strerror", "fa_version", "fa_watchdog_selftest"]
 
 
@@ -172,3 +172,43 @@ def test_rect_entry_checks_arguments(fa):
     if not torch.cuda.is_available():  # past the host checks the call reaches the device
         rc = raw(Q, K, V, Q + qb, L, 1, 2, 64, 512, 64, 0, 0.125, None)  # just past q: no alias
         assert rc != fa.FA_ERR_ALIAS
+
+
+def test_bwd_entry_checks_arguments(fa):
+    raw = fa.lib().fa_bwd
+    # q, o, do, dq: [1][2][64][64]; k, v, dk, dv: [1][2][512][64]
+    qb, kb = 1 * 2 * 64 * 64 * 2, 1 * 2 * 512 * 64 * 2
+    DO, DQ, DK, DV = (A + i * STEP for i in range(5, 9))
+    args = [Q, K, V, O, L, DO, DQ, DK, DV]
+
+    def call(*ptrs, B=1, H=2, Nq=64, Nk=512, d=64, causal=0, scale=0.125):
+        return raw(*ptrs, B, H, Nq, Nk, d, causal, scale, None)
+
+    assert call(*args, Nq=0) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, Nk=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, d=96) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, causal=3) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, Nk=128 * 65536) == fa.FA_ERR_INVALID_ARG   # more key blocks than the grid takes
+    for i in range(9):
+        bad = list(args)
+        bad[i] = None
+        assert call(*bad) == fa.FA_ERR_NULL, i
+    for i in range(9):
+        bad = list(args)
+        bad[i] = args[i] + (2 if i == 4 else 8)
+        assert call(*bad) == fa.FA_ERR_ALIGN, i
+    # every output against every input and the other outputs
+    bad = list(args)
+    bad[6] = O + qb - 16                      # dq over the tail of o
+    assert call(*bad) == fa.FA_ERR_ALIAS
+    bad = list(args)
+    bad[7] = V + kb - 16                      # dk over the tail of v
+    assert call(*bad) == fa.FA_ERR_ALIAS
+    bad = list(args)
+    bad[8] = DK + 16                          # dv over dk
+    assert call(*bad) == fa.FA_ERR_ALIAS
+    bad = list(args)
+    bad[8] = L                                # dv over lse
+    assert call(*bad) == fa.FA_ERR_ALIAS
