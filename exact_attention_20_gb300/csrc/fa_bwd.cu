@@ -86,8 +86,7 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* o, c
   const long long BH = static_cast<long long>(B) * H;
   const long long nq_pad = (static_cast<long long>(Nq) + 63) / 64 * 64;
   if (BH * nq_pad * d >= (1ll << 31) || BH * Nk * d >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-  if ((static_cast<long long>(Nk) + fa::bwd::kBlockK - 1) / fa::bwd::kBlockK > 65535)
-    return FA_ERR_INVALID_ARG;
+  if (BH > 65535) return FA_ERR_INVALID_ARG;  // the grid's y dimension
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
   auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   for (const void* p : {q, k, v, o, dout, dq, dk, dv})
@@ -123,12 +122,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   float* lp = reinterpret_cast<float*>(ws + lay.lp);
   float* dsum = reinterpret_cast<float*>(ws + lay.dsum);
 
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo;
   if (!fa::encode_bf16_3d(&tq, q, D, Nq, BH, 64, fa::bwd::kBlockQ) ||
       !fa::encode_bf16_3d(&tdo, dout, D, Nq, BH, 64, fa::bwd::kBlockQ) ||
       !fa::encode_bf16_3d(&tk, k, D, Nk, BH, 64, fa::bwd::kBlockK) ||
-      !fa::encode_bf16_3d(&tv, v, D, Nk, BH, 64, fa::bwd::kBlockK) ||
-      !fa::encode_f32_3d(&tdq, acc, D, Nq, BH, 32, fa::bwd::kBlockQ))
+      !fa::encode_bf16_3d(&tv, v, D, Nk, BH, 64, fa::bwd::kBlockK))
     return FA_ERR_LAUNCH;
   {
     std::lock_guard<std::mutex> lock(g_mu);
@@ -150,6 +148,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
 
   fa::bwd::BwdParams p;
+  p.dq_acc = acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.lp = lp;
@@ -163,7 +162,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.scale = scale;
   p.wait_limit_ns = fa_internal::kWaitLimitNs;
   fa::bwd::fa_bwd_kernel<D, CAUSAL>
-      <<<dim3(BH, n_kb), fa::bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+      <<<dim3(n_kb, BH), fa::bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
 
   const long long n8 = static_cast<long long>(BH) * Nq * D / 8;

@@ -20,24 +20,32 @@
 //   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d
 //   dP^T = V dO^T     same shape
 //   dV  += P^T dO     M = 128 keys, N = d, K = 64 queries (P^T read from TMEM)
-//   dK  += dS^T Q     same shape (dS^T read from shared memory)
-//   dQ^T = K^T dS^T   M = d (128 lanes), N = 64 queries, K = 128 keys
+//   dK  += dS^T Q     same shape (dS^T read from TMEM)
+//   dQ^T = K^T dS^T   M = d (128 lanes), N = 64 queries, K = 128 keys (dS^T
+//                     read from shared memory)
 // Every key block adds to every query row's dQ, so each step's dQ^T is added
-// into an fp32 accumulator in global memory by TMA reductions (the adds are
-// done by the memory system, not by atomics from threads).  With d = 64 the
-// dQ^T product still has M = 128: rows 64-127 of its A operand are V^T (the
-// tile that follows K in shared memory) and those lanes are ignored.
+// into an fp32 accumulator in global memory by reductions from registers
+// (red.global.add: the adds are done in L2).  With d = 64 the dQ^T product
+// still has M = 128: rows 64-127 of its A operand are V^T (the tile that
+// follows K in shared memory) and those lanes are ignored.
+//
+// The tensor core reads both operands of a product from shared memory unless
+// A comes from TMEM, and at M = 128 that read, not the arithmetic, sets the
+// pace of the N = 64 products; so P^T and dS^T, made by the threads, are
+// handed to the tensor core in TMEM where they are an A operand.
 //
 // Warp roles (12 warps, 384 threads):
 //   warp 0     TMA producer: K and V once; Q, dO and their rows' L and D per step
 //   warp 1     MMA issuer (one lane issues), owner of the TMEM allocation
 //   warps 2-3  idle
 //   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
-//   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread
+//   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread, reduced
+//              into the fp32 accumulator
 // Tensor memory (fp32 columns): S^T in two buffers at 0 and 64, dP^T at 128,
-// dQ^T at 192, dV at 256, dK at 384.  P^T (bf16, two per column) overwrites
-// the first 32 columns of its S^T buffer.  S^T has two buffers so that the
-// next step's S^T is computed while this step's P^T still feeds dV.
+// dQ^T at 192, dV at 256, dK at 384.  P^T and dS^T (bf16, two per column)
+// overwrite the first and the second 32 columns of their S^T buffer.  S^T has
+// two buffers so that the next step's S^T is computed while this step's P^T
+// and dS^T still feed dV and dK.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -50,7 +58,6 @@ namespace bwd {
 constexpr int kBlockK = 128;   // keys per CTA
 constexpr int kBlockQ = 64;    // query rows per step
 constexpr int kThreads = 384;
-constexpr int kStages = 2;     // Q / dO ring depth
 constexpr int kLoadWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kDsWarp0 = 4;    // first warp of the P / dS warpgroup
@@ -71,6 +78,9 @@ constexpr int kSiteDrain = 14;
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+  // Q / dO ring depth: a step's tiles are requested two steps ahead (three
+  // at d = 64); at d = 128 a fourth stage would not fit in shared memory.
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kKSlab = kBlockK * 128;  // 128 rows x 64 bf16 (one TMA box)
   static constexpr int kQSlab = kBlockQ * 128;  // 64 rows x 64 bf16
   static constexpr int kKTile = (D / 64) * kKSlab;
@@ -81,13 +91,10 @@ struct Cfg {
   static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
   static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries]
-  static constexpr int kDqOff = kDsOff + 2 * kDsBytes;
-  static constexpr int kDqWarpBytes = kBlockQ * 32 * 4;   // one drain warp: [64 rows][32 d] fp32
-  static constexpr int kDqBytes = (D / 32) * kDqWarpBytes;
-  static constexpr int kLdOff = kDqOff + kDqBytes;        // per stage: L[64] then D[64], fp32
+  static constexpr int kLdOff = kDsOff + 2 * kDsBytes;    // per stage: L[64] then D[64], fp32
   static constexpr int kLdBytes = 2 * kBlockQ * 4;
   static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 10 + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStageBytes % 1024 == 0,
@@ -96,6 +103,7 @@ struct Cfg {
 };
 
 struct BwdParams {
+  float* dq_acc;          // workspace [BH][Nq][D] fp32, zero on entry; dQ / scale on exit
   __nv_bfloat16* dk;      // [BH][Nk][D]
   __nv_bfloat16* dv;      // [BH][Nk][D]
   const float* lp;        // workspace [BH][Nq_pad]: L * log2(e); +inf on padding rows
@@ -141,16 +149,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   }
 }
 
-// 3-D tiled reduction into global memory: tensor[...] += the shared-memory
-// box at `src` (element type and box from the tensor map); elements outside
-// the tensor are skipped.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
-                                                  int32_t c1, int32_t c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
+// dst += v in global memory, performed in L2 (no value returned).
+__device__ __forceinline__ void red_add_f32(float* dst, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -174,8 +175,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
   }
   int it = 0;
   for (; it < n; ++it) {
-    const int st = it & 1;
-    if (!wait_phase(sy.stage_empty(st), ((it >> 1) & 1) ^ 1, sy, p, kSiteProducer)) break;
+    const int st = it % C::kStages;
+    if (!wait_phase(sy.stage_empty(st), ((it / C::kStages) & 1) ^ 1, sy, p, kSiteProducer)) break;
     const int q0 = (j0 + it) * kBlockQ;
     const uint32_t full = sy.stage_full(st);
     mbar_arrive_expect_tx(full, C::kStageBytes + C::kLdBytes);
@@ -194,8 +195,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
   }
   // Drain: every copy this thread started lands before the CTA exits.
   mbar_wait_bounded(sy.kv_full, 0, p.wait_limit_ns);
-  for (int c = it > 2 ? it - 2 : 0; c < it; ++c)
-    mbar_wait_bounded(sy.stage_full(c & 1), (c >> 1) & 1, p.wait_limit_ns);
+  for (int c = it > C::kStages ? it - C::kStages : 0; c < it; ++c)
+    mbar_wait_bounded(sy.stage_full(c % C::kStages), (c / C::kStages) & 1, p.wait_limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -213,7 +214,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
 template <int D>
 struct Desc {
   using C = Cfg<D>;
-  uint64_t k_kmaj, v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_kmaj0, ds_mn0;
+  uint64_t k_kmaj, v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_mn0;
   __device__ __forceinline__ explicit Desc(uint32_t sbase) {
     k_kmaj = sdesc_sw128(sbase + C::kKOff, 16, 1024);
     v_kmaj = sdesc_sw128(sbase + C::kVOff, 16, 1024);
@@ -224,14 +225,12 @@ struct Desc {
     q_mn0 = sdesc_sw128(st, C::kQSlab, 1024);
     do_mn0 = sdesc_sw128(st + C::kQTile, C::kQSlab, 1024);
     const uint32_t ds = sbase + C::kDsOff;
-    ds_kmaj0 = sdesc_sw128(ds, 16, 1024);
     ds_mn0 = sdesc_sw128(ds, C::kDsBytes, 1024);  // N = 64: one slab, the leading offset is not used
   }
   __device__ __forceinline__ uint64_t q_kmaj(int b) const { return sdesc_advance(q_kmaj0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t do_kmaj(int b) const { return sdesc_advance(do_kmaj0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t q_mn(int b) const { return sdesc_advance(q_mn0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t do_mn(int b) const { return sdesc_advance(do_mn0, b * C::kStageBytes); }
-  __device__ __forceinline__ uint64_t ds_kmaj(int b) const { return sdesc_advance(ds_kmaj0, b * C::kDsBytes); }
   __device__ __forceinline__ uint64_t ds_mn(int b) const { return sdesc_advance(ds_mn0, b * C::kDsBytes); }
 };
 
@@ -250,6 +249,7 @@ __device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint64_t a, uint64
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy,
                                         const BwdParams& p, int n) {
+  using C = Cfg<D>;
   const bool leader = (threadIdx.x & 31) == 0;
   bool ok = true;
   auto wait_voted = [&](uint32_t bar, uint32_t par) {
@@ -275,16 +275,18 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     }
   }
   for (int it = 0; it < n && ok; ++it) {
-    const int b = it & 1;
+    const int b = it & 1;                 // S^T and dS^T buffer
+    const int st = it % C::kStages;       // Q / dO stage
+    const int st1 = (it + 1) % C::kStages;
     const bool more = it + 1 < n;
     if (more) {
-      // S^T of the next step into the other buffer: its previous P^T fed the
-      // dV product of step it-1, issued before this one.
-      wait_voted(sy.stage_full(b ^ 1), ((it + 1) >> 1) & 1);
+      // S^T of the next step into the other buffer: its previous P^T and
+      // dS^T fed the dV and dK products of step it-1, issued before this one.
+      wait_voted(sy.stage_full(st1), ((it + 1) / C::kStages) & 1);
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {
-        issue_scores<D>(tmem + kColS + (b ^ 1) * 64, ds.k_kmaj, ds.q_kmaj(b ^ 1));
+        issue_scores<D>(tmem + kColS + (b ^ 1) * 64, ds.k_kmaj, ds.q_kmaj(st1));
         umma_commit(sy.s_full(b ^ 1));
       }
       __syncwarp();
@@ -294,17 +296,17 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     tc_fence_after_sync();
     if (leader) {
       if (more) {
-        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(b ^ 1));
+        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(st1));
         umma_commit(sy.dp_full);
       }
       const uint32_t acc = it > 0 ? 1u : 0u;
 #pragma unroll
       for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dV += P^T dO
-        umma_ts(tm_dv, tmem + kColS + b * 64 + kk * 8, sdesc_advance(ds.do_mn(b), kk * 2048), id_acc,
+        umma_ts(tm_dv, tmem + kColS + b * 64 + kk * 8, sdesc_advance(ds.do_mn(st), kk * 2048), id_acc,
                 kk > 0 ? 1u : acc);
 #pragma unroll
       for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
-        umma_ss(tm_dk, sdesc_advance(ds.ds_kmaj(b), kk * 32), sdesc_advance(ds.q_mn(b), kk * 2048), id_acc,
+        umma_ts(tm_dk, tmem + kColS + b * 64 + 32 + kk * 8, sdesc_advance(ds.q_mn(st), kk * 2048), id_acc,
                 kk > 0 ? 1u : acc);
     }
     __syncwarp();
@@ -317,7 +319,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
         umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
                 kk > 0 ? 1u : 0u);
       umma_commit(sy.dq_full);
-      umma_commit(sy.stage_empty(b));
+      umma_commit(sy.stage_empty(st));
       umma_commit(sy.ds_free(b));
     }
     __syncwarp();
@@ -346,13 +348,14 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
   bool ok = true;
   for (int it = 0; it < n; ++it) {
     const int b = it & 1;
+    const int st = it % C::kStages;
     const int q0 = (j0 + it) * kBlockQ;
     bool w = wait_phase(sy.s_full(b), (it >> 1) & 1, sy, p, kSiteDs);
-    w = w && wait_phase(sy.stage_full(b), (it >> 1) & 1, sy, p, kSiteDs);  // L, D of the step
+    w = w && wait_phase(sy.stage_full(st), (it / C::kStages) & 1, sy, p, kSiteDs);  // L, D of the step
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after_sync();
-    const float* Lrow = reinterpret_cast<const float*>(smem + C::kLdOff + b * C::kLdBytes);
+    const float* Lrow = reinterpret_cast<const float*>(smem + C::kLdOff + st * C::kLdBytes);
     const float* Drow = Lrow + kBlockQ;
     const uint32_t tS = tmem + lane_off + kColS + b * 64;
 
@@ -391,8 +394,10 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
       tmem_st32(tS, pk);
     }
 
-    // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16 and written to the
-    // 128-byte-swizzled dS^T tile (16-byte chunk ch of row r at chunk ch ^ (r % 8)).
+    // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16, stored to tensor
+    // memory after P^T (the A operand of dK) and to the 128-byte-swizzled dS^T
+    // tile in shared memory (the B operand of dQ^T; 16-byte chunk ch of row r
+    // at chunk ch ^ (r % 8)).
     w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
     if (it >= 2) w = w && wait_phase(sy.ds_free(b), ((it >> 1) - 1) & 1, sy, p, kSiteDs);
     ok = __all_sync(0xffffffffu, w);
@@ -418,8 +423,9 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
         *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) * 16)) =
             make_uint4(wds[4 * q], wds[4 * q + 1], wds[4 * q + 2], wds[4 * q + 3]);
       }
+      tmem_st16(tS + 32 + h * 16, wds);
     }
-    tmem_st_wait();            // P^T is in tensor memory
+    tmem_st_wait();            // P^T and dS^T are in tensor memory
     fence_proxy_async_smem();  // dS^T is visible to the tensor core
     tc_fence_before_sync();
     __syncwarp();
@@ -464,24 +470,18 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
 // ---------------------------------------------------------------------------
 // dQ drain (warps 8-11): thread = one row of dQ^T (one column of d)
 // ---------------------------------------------------------------------------
-// Each warp owns 32 columns of d.  Per step it moves its [64 queries][32]
-// block of dQ^T from tensor memory into its own staging area (row-major, so
-// a warp's store covers 128 contiguous bytes) and adds it into the fp32 dQ
-// accumulator with one TMA reduction; rows past the last query are outside
-// the tensor map and skipped.  With d = 64 only warps 8 and 9 hold dQ^T rows.
+// Per step each thread adds its 64 values of dQ^T (one column of d, 64 query
+// rows) into the fp32 accumulator, one reduction per query row: a warp's
+// reduction covers 32 consecutive floats (128 bytes) of one row.  Rows past
+// the last query are skipped.  With d = 64 only warps 8 and 9 hold dQ^T rows.
 template <int D>
-__device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t sbase, uint32_t tmem,
-                                          const CUtensorMap* tmDq, const Sync& sy, const BwdParams& p,
-                                          int bh, int j0, int n) {
-  using C = Cfg<D>;
+__device__ __forceinline__ void run_drain(uint32_t tmem, const Sync& sy, const BwdParams& p, int bh, int j0,
+                                          int n) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const bool has_rows = quad * 32 < D;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-  float* stage = reinterpret_cast<float*>(smem + C::kDqOff + (has_rows ? quad : 0) * C::kDqWarpBytes);
-  const uint32_t stage_s = sbase + C::kDqOff + (has_rows ? quad : 0) * C::kDqWarpBytes;
-  bool issued = false;
   for (int it = 0; it < n; ++it) {
     const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full, it & 1, sy, p, kSiteDrain));
     if (!ok) break;
@@ -492,31 +492,29 @@ __device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t sbase, uint32_
     __syncwarp();
     if (lane == 0) mbar_arrive(sy.dq_free);
     if (!has_rows) continue;
-    if (lane == 0 && issued) tma_store_wait_read0();  // the last reduction has read the staging area
-    __syncwarp();
+    const int q0 = (j0 + it) * kBlockQ;
+    const int rows = min(kBlockQ, p.Nq - q0);
+    float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + q0) * D + quad * 32 + lane;
+    if (rows == kBlockQ) {
 #pragma unroll
-    for (int q = 0; q < kBlockQ; ++q) stage[q * 32 + lane] = __uint_as_float(x[q]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_reduce_add_3d(tmDq, stage_s, quad * 32, (j0 + it) * kBlockQ, bh);
-      tma_store_commit();
-      issued = true;
+      for (int c = 0; c < kBlockQ; ++c) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(x[c]));
+    } else {
+#pragma unroll
+      for (int c = 0; c < kBlockQ; ++c)
+        if (c < rows) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(x[c]));
     }
-    __syncwarp();
   }
-  if (lane == 0 && issued) tma_store_wait_all0();
 }
 
 // ---------------------------------------------------------------------------
-// Kernel: grid (B*H, key blocks); key block 0 (the longest under the causal
-// mask) of every head is scheduled first
+// Kernel: grid (key blocks, B*H).  The CTAs of one head are adjacent in launch
+// order, so the ones running together share their heads' Q and dO tiles in L2.
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ CUtensorMap tmDq, const BwdParams p) {
+              const BwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -524,8 +522,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int kb = blockIdx.y;
+  const int kb = blockIdx.x;
+  const int bh = blockIdx.y;
   // Query steps of this key block: under the top-left causal mask key j is
   // seen by queries i >= j, so the first step is the one holding query kb*128.
   const int j0 = CAUSAL ? (kb * kBlockK) / kBlockQ : 0;
@@ -537,9 +535,9 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     auto next = [&]() { const uint32_t r = b; b += 8; return r; };
     sy.kv_full = next();
     sy.stage_full0 = next();
-    next();
+    for (int i = 1; i < C::kStages; ++i) next();
     sy.stage_empty0 = next();
-    next();
+    for (int i = 1; i < C::kStages; ++i) next();
     sy.s_full0 = next();
     next();
     sy.dp_full = next();
@@ -555,9 +553,11 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     mbar_init(sy.kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(sy.stage_full(i), 1);
       mbar_init(sy.stage_empty(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(sy.s_full(i), 1);
       mbar_init(sy.ds_free(i), 1);
     }
@@ -575,7 +575,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
   }
-  if (warp == kDrainWarp0 && lane == 0) tma_prefetch_desc(&tmDq);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish_alloc_permit();
@@ -593,7 +592,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else if (warp >= kDsWarp0 && warp < kDsWarp0 + 4) {
     run_ds<D, CAUSAL>(smem, tmem, sy, p, bh, kb, j0, n);
   } else if (warp >= kDrainWarp0) {
-    run_drain<D>(smem, sbase, tmem, &tmDq, sy, p, bh, j0, n);
+    run_drain<D>(tmem, sy, p, bh, j0, n);
   }
 
   tc_fence_before_sync();

@@ -166,7 +166,7 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
  *   dk, dv     : bf16 [B][H][Nk][d]; written.  No output may overlap an input or another output.
  *   B, H, Nq, Nk, d, causal, scale : as for fa_fwd_rect (the same values the
  *             forward used; causal is the top-left mask), with
- *             B*H*ceil(Nq/64)*64*d < 2^31, B*H*Nk*d < 2^31 and ceil(Nk/128) <= 65535.
+ *             B*H*ceil(Nq/64)*64*d < 2^31, B*H*Nk*d < 2^31 and B*H <= 65535.
  *   stream     : cudaStream_t as void*.
  *
  * The method is the recompute-from-L backward of "FlashAttention and
@@ -176,8 +176,9 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
  * dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.  P and dS are rounded
  * to bf16 before their products; every product accumulates in fp32; the
  * outputs are rounded once to bf16.  dQ sums the contributions of all key
- * blocks in an fp32 accumulator in the order the blocks finish, so its last
- * bit may differ between runs; dK and dV are deterministic.
+ * blocks in an fp32 accumulator (reductions performed in L2) in the order
+ * they arrive, so its last bit may differ between runs; dK and dV are
+ * deterministic.
  *
  * Three launches on `stream`: prep (D, L in log2 units, accumulator zeroed),
  * the backward kernel (one CTA per (b, h, 128-key block)), and the dQ

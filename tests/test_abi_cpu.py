@@ -190,7 +190,7 @@ def test_bwd_entry_checks_arguments(fa):
     assert call(*args, causal=3) == fa.FA_ERR_INVALID_ARG
     assert call(*args, scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert call(*args, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
-    assert call(*args, Nk=128 * 65536) == fa.FA_ERR_INVALID_ARG   # more key blocks than the grid takes
+    assert call(*args, B=65536, H=1, Nq=1, Nk=1) == fa.FA_ERR_INVALID_ARG   # more heads than the grid takes
     for i in range(9):
         bad = list(args)
         bad[i] = None
