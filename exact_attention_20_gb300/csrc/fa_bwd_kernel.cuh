@@ -17,7 +17,7 @@
 // memory for the whole launch, and walks the query rows 64 at a time (a
 // step).  Every product is taken transposed so that the 128 keys are the
 // tensor-memory lanes and one thread owns one key row:
-//   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d
+//   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d (K read from TMEM)
 //   dP^T = V dO^T     same shape
 //   dV  += P^T dO     M = 128 keys, N = d, K = 64 queries (P^T read from TMEM)
 //   dK  += dS^T Q     same shape (dS^T read from TMEM)
@@ -31,21 +31,25 @@
 //
 // The tensor core reads both operands of a product from shared memory unless
 // A comes from TMEM, and at M = 128 that read, not the arithmetic, sets the
-// pace of the N = 64 products; so P^T and dS^T, made by the threads, are
-// handed to the tensor core in TMEM where they are an A operand.
+// pace of the N = 64 products and starves every other shared-memory access;
+// so K (the same for every step) and P^T and dS^T (made by the threads) are
+// handed to the tensor core in TMEM wherever they are an A operand.
 //
 // Warp roles (12 warps, 384 threads):
 //   warp 0     TMA producer: K and V once; Q, dO and their rows' L and D per step
 //   warp 1     MMA issuer (one lane issues), owner of the TMEM allocation
 //   warps 2-3  idle
-//   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
+//   warps 4-7  K into TMEM once; P and dS, one key row per thread; the dK,
+//              dV epilogue
 //   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread, reduced
 //              into the fp32 accumulator
-// Tensor memory (fp32 columns): S^T in two buffers at 0 and 64, dP^T at 128,
-// dQ^T at 192, dV at 256, dK at 384.  P^T and dS^T (bf16, two per column)
-// overwrite the first and the second 32 columns of their S^T buffer.  S^T has
-// two buffers so that the next step's S^T is computed while this step's P^T
-// and dS^T still feed dV and dK.
+// Tensor memory (32-bit columns): K (bf16, two per column) at 0, S^T in two
+// buffers at 64 and 128, dP^T at 192, dV at 256, dK at 384.  P^T and dS^T
+// (bf16) overwrite the first and the second 32 columns of their S^T buffer;
+// S^T has two buffers so that the S^T of a later step is computed while this
+// step's P^T and dS^T still feed dV and dK.  dQ^T goes to dP^T's columns once
+// the threads have read dP^T, and the next dP^T waits until the drain has
+// read dQ^T.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -63,9 +67,10 @@ constexpr int kMmaWarp = 1;
 constexpr int kDsWarp0 = 4;    // first warp of the P / dS warpgroup
 constexpr int kDrainWarp0 = 8; // first warp of the dQ drain warpgroup
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // + 64 * buffer
-constexpr uint32_t kColDP = 128;
-constexpr uint32_t kColDQ = 192;
+constexpr uint32_t kColK = 0;
+constexpr uint32_t kColS = 64;   // + 64 * buffer
+constexpr uint32_t kColDP = 192;
+constexpr uint32_t kColDQ = kColDP;
 constexpr uint32_t kColDV = 256;
 constexpr uint32_t kColDK = 384;
 
@@ -74,13 +79,17 @@ constexpr int kSiteProducer = 11;
 constexpr int kSiteMma = 12;
 constexpr int kSiteDs = 13;
 constexpr int kSiteDrain = 14;
+constexpr int kSiteAlign = 15;  // dynamic shared memory not 1024-byte aligned
+// Steps ahead of the one being loaded whose Q and dO tiles (and L, D) are
+// prefetched into L2: the CTAs of a head walk the same steps at about the
+// same time, and a tile's first request would otherwise wait on DRAM.
+constexpr int kPrefetchSteps = 4;
 
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  // Q / dO ring depth: a step's tiles are requested two steps ahead (three
-  // at d = 64); at d = 128 a fourth stage would not fit in shared memory.
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  // Q / dO ring depth: a step's tiles are requested three steps ahead.
+  static constexpr int kStages = 4;
   static constexpr int kKSlab = kBlockK * 128;  // 128 rows x 64 bf16 (one TMA box)
   static constexpr int kQSlab = kBlockQ * 128;  // 64 rows x 64 bf16
   static constexpr int kKTile = (D / 64) * kKSlab;
@@ -91,12 +100,15 @@ struct Cfg {
   static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
   static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries]
-  static constexpr int kLdOff = kDsOff + 2 * kDsBytes;    // per stage: L[64] then D[64], fp32
+  static constexpr int kLdOff = kDsOff + kDsBytes;        // per stage: L[64] then D[64], fp32
   static constexpr int kLdBytes = 2 * kBlockQ * 4;
   static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
-  static constexpr int kNumBars = 10 + 2 * kStages;
+  static constexpr int kNumBars = 9 + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  // No alignment slack: the dynamic shared memory of a CTA starts on a
+  // 1024-byte boundary (after the 1 KB the system reserves); the kernel checks
+  // this and gives up (status word) if it ever does not.
+  static constexpr int kSmemBytes = kMiscOff + 16;
   static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStageBytes % 1024 == 0,
                 "operand tiles must sit on 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -119,14 +131,15 @@ struct BwdParams {
 // Barrier addresses.  The pairs (one per stage or buffer) are adjacent, so
 // buffer b's barrier is the pair's address + 8 b (no run-time array index,
 // which would put the struct in local memory).
+// dq_full completes once per step, when that step's dQ^T product is done:
+// the drain then reads dQ^T, and the dS^T tile the product read may be
+// written again.
 struct Sync {
-  uint32_t kv_full, stage_full0, stage_empty0, s_full0, dp_full, sm_done, dq_full, dq_free, ds_free0,
-      acc_done;
+  uint32_t kv_full, k_ready, stage_full0, stage_empty0, s_full0, dp_full, sm_done, dq_full, dq_free, acc_done;
   volatile int* abort_flag;
   __device__ __forceinline__ uint32_t stage_full(int b) const { return stage_full0 + 8 * b; }
   __device__ __forceinline__ uint32_t stage_empty(int b) const { return stage_empty0 + 8 * b; }
   __device__ __forceinline__ uint32_t s_full(int b) const { return s_full0 + 8 * b; }
-  __device__ __forceinline__ uint32_t ds_free(int b) const { return ds_free0 + 8 * b; }
 };
 
 // Bounded wait: true when the phase completed; false if this CTA is aborting
@@ -173,9 +186,22 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
     tma_load_3d_hint(sbase + C::kKOff + s * C::kKSlab, tmK, sy.kv_full, s * 64, kb * kBlockK, bh, pol_kv);
     tma_load_3d_hint(sbase + C::kVOff + s * C::kKSlab, tmV, sy.kv_full, s * 64, kb * kBlockK, bh, pol_kv);
   }
+  auto prefetch_step = [&](int s) {
+    const int q0 = (j0 + s) * kBlockQ;
+#pragma unroll
+    for (int x = 0; x < D / 64; ++x) {
+      tma_prefetch_3d(tmQ, x * 64, q0, bh);
+      tma_prefetch_3d(tmDO, x * 64, q0, bh);
+    }
+    const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad + q0;
+    prefetch_l2_bulk(p.lp + row0, kBlockQ * 4);
+    prefetch_l2_bulk(p.dsum + row0, kBlockQ * 4);
+  };
+  for (int s = 0; s < kPrefetchSteps + C::kStages && s < n; ++s) prefetch_step(s);
   int it = 0;
   for (; it < n; ++it) {
     const int st = it % C::kStages;
+    if (it + kPrefetchSteps + C::kStages < n) prefetch_step(it + kPrefetchSteps + C::kStages);
     if (!wait_phase(sy.stage_empty(st), ((it / C::kStages) & 1) ^ 1, sy, p, kSiteProducer)) break;
     const int q0 = (j0 + it) * kBlockQ;
     const uint32_t full = sy.stage_full(st);
@@ -214,9 +240,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
 template <int D>
 struct Desc {
   using C = Cfg<D>;
-  uint64_t k_kmaj, v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_mn0;
+  uint64_t v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_mn0;
   __device__ __forceinline__ explicit Desc(uint32_t sbase) {
-    k_kmaj = sdesc_sw128(sbase + C::kKOff, 16, 1024);
     v_kmaj = sdesc_sw128(sbase + C::kVOff, 16, 1024);
     kt_mn = sdesc_sw128(sbase + C::kKOff, C::kKSlab, 1024);
     const uint32_t st = sbase + C::kStageOff;
@@ -231,19 +256,30 @@ struct Desc {
   __device__ __forceinline__ uint64_t do_kmaj(int b) const { return sdesc_advance(do_kmaj0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t q_mn(int b) const { return sdesc_advance(q_mn0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t do_mn(int b) const { return sdesc_advance(do_mn0, b * C::kStageBytes); }
-  __device__ __forceinline__ uint64_t ds_mn(int b) const { return sdesc_advance(ds_mn0, b * C::kDsBytes); }
 };
 
-// S^T = K Q^T or dP^T = V dO^T: A = the 128-key tile, B = the 64-row tile,
-// both K-major over d.
+// dP^T = V dO^T: A = the V tile (128 keys), B = the dO tile (64 rows), both
+// K-major over d in shared memory.
 template <int D>
-__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint64_t a, uint64_t b) {
+__device__ __forceinline__ void issue_dp(uint32_t d_tmem, uint64_t a, uint64_t b) {
   using C = Cfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32_ab(kBlockK, kBlockQ, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk)
     umma_ss(d_tmem, sdesc_advance(a, (kk / 4) * C::kKSlab + (kk % 4) * 32),
             sdesc_advance(b, (kk / 4) * C::kQSlab + (kk % 4) * 32), idesc, kk > 0 ? 1u : 0u);
+}
+
+// S^T = K Q^T: A = K from tensor memory (16 values of d = 8 columns per
+// instruction), B = the Q tile, K-major over d in shared memory.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64_t b) {
+  using C = Cfg<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32_ab(kBlockK, kBlockQ, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    umma_ts(d_tmem, k_tmem + kk * 8, sdesc_advance(b, (kk / 4) * C::kQSlab + (kk % 4) * 32), idesc,
+            kk > 0 ? 1u : 0u);
 }
 
 template <int D, bool CAUSAL>
@@ -260,69 +296,92 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
   const uint32_t tm_dv = tmem + kColDV, tm_dk = tmem + kColDK;
   constexpr uint32_t id_acc = idesc_bf16_f32_ab(kBlockK, D, false, true);      // dV, dK
   constexpr uint32_t id_dq = idesc_bf16_f32_ab(128, kBlockQ, true, true);      // dQ^T
+  // Order of the products (step it uses S^T buffer b = it % 2 and Q / dO
+  // stage it % kStages):
+  //   before the loop:  S^T(0), dP^T(0), S^T(1)
+  //   step it:          [P^T, dS^T of step it ready]  dQ^T(it)  dV(it)
+  //                     [drain has read dQ^T(it)]     dP^T(it+1)  dK(it)
+  //                     S^T(it+2) into buffer b
+  // dQ^T(it) overwrites dP^T(it), which the threads have read; dP^T(it+1) is
+  // what the threads wait on next, so it goes out as soon as the drain has
+  // emptied the columns, behind dV(it) which covers the drain's read.
   wait_voted(sy.kv_full, 0);
+  wait_voted(sy.k_ready, 0);  // K in tensor memory
+  auto stage_ready = [&](int step) {
+    wait_voted(sy.stage_full(step % C::kStages), (step / C::kStages) & 1);
+  };
   if (n > 0 && ok) {
-    wait_voted(sy.stage_full(0), 0);
+    stage_ready(0);
     if (ok) {
       tc_fence_after_sync();
       if (leader) {
-        issue_scores<D>(tmem + kColS, ds.k_kmaj, ds.q_kmaj(0));
+        issue_s<D>(tmem + kColS, tmem + kColK, ds.q_kmaj(0));
         umma_commit(sy.s_full(0));
-        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(0));
+        issue_dp<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(0));
         umma_commit(sy.dp_full);
       }
       __syncwarp();
+    }
+    if (n > 1 && ok) {
+      stage_ready(1);
+      if (ok) {
+        tc_fence_after_sync();
+        if (leader) {
+          issue_s<D>(tmem + kColS + 64, tmem + kColK, ds.q_kmaj(1));
+          umma_commit(sy.s_full(1));
+        }
+        __syncwarp();
+      }
     }
   }
   for (int it = 0; it < n && ok; ++it) {
-    const int b = it & 1;                 // S^T and dS^T buffer
+    const int b = it & 1;                 // S^T buffer (P^T, dS^T in TMEM)
     const int st = it % C::kStages;       // Q / dO stage
-    const int st1 = (it + 1) % C::kStages;
-    const bool more = it + 1 < n;
-    if (more) {
-      // S^T of the next step into the other buffer: its previous P^T and
-      // dS^T fed the dV and dK products of step it-1, issued before this one.
-      wait_voted(sy.stage_full(st1), ((it + 1) / C::kStages) & 1);
-      if (!ok) break;
-      tc_fence_after_sync();
-      if (leader) {
-        issue_scores<D>(tmem + kColS + (b ^ 1) * 64, ds.k_kmaj, ds.q_kmaj(st1));
-        umma_commit(sy.s_full(b ^ 1));
-      }
-      __syncwarp();
-    }
-    wait_voted(sy.sm_done, it & 1);  // P^T in TMEM, dS^T in shared memory; S^T, dP^T read
+    const uint32_t tm_s = tmem + kColS + b * 64;
+    wait_voted(sy.sm_done, it & 1);  // P^T, dS^T in TMEM, dS^T in shared memory; S^T, dP^T read
     if (!ok) break;
     tc_fence_after_sync();
-    if (leader) {
-      if (more) {
-        issue_scores<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(st1));
-        umma_commit(sy.dp_full);
-      }
-      const uint32_t acc = it > 0 ? 1u : 0u;
-#pragma unroll
-      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dV += P^T dO
-        umma_ts(tm_dv, tmem + kColS + b * 64 + kk * 8, sdesc_advance(ds.do_mn(st), kk * 2048), id_acc,
-                kk > 0 ? 1u : acc);
-#pragma unroll
-      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
-        umma_ts(tm_dk, tmem + kColS + b * 64 + 32 + kk * 8, sdesc_advance(ds.q_mn(st), kk * 2048), id_acc,
-                kk > 0 ? 1u : acc);
-    }
-    __syncwarp();
-    if (it > 0) wait_voted(sy.dq_free, (it - 1) & 1);  // the drain has read dQ^T of the last step
-    if (!ok) break;
-    tc_fence_after_sync();
+    const uint32_t acc = it > 0 ? 1u : 0u;
     if (leader) {
 #pragma unroll
       for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T
-        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
+        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn0, kk * 2048), id_dq,
                 kk > 0 ? 1u : 0u);
       umma_commit(sy.dq_full);
-      umma_commit(sy.stage_empty(st));
-      umma_commit(sy.ds_free(b));
+#pragma unroll
+      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dV += P^T dO
+        umma_ts(tm_dv, tm_s + kk * 8, sdesc_advance(ds.do_mn(st), kk * 2048), id_acc, kk > 0 ? 1u : acc);
     }
     __syncwarp();
+    if (it + 1 < n) {
+      wait_voted(sy.dq_free, it & 1);  // the drain has read dQ^T(it)
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_dp<D>(tm_dp, ds.v_kmaj, ds.do_kmaj((it + 1) % C::kStages));
+        umma_commit(sy.dp_full);
+      }
+      __syncwarp();
+    }
+    if (leader) {
+#pragma unroll
+      for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
+        umma_ts(tm_dk, tm_s + 32 + kk * 8, sdesc_advance(ds.q_mn(st), kk * 2048), id_acc, kk > 0 ? 1u : acc);
+      umma_commit(sy.stage_empty(st));  // the step's Q and dO are no longer read
+    }
+    __syncwarp();
+    if (it + 2 < n) {
+      // S^T(it+2) into buffer b: P^T(it) and dS^T(it) there were read by
+      // dV(it) and dK(it), issued before it
+      stage_ready(it + 2);
+      if (!ok) break;
+      tc_fence_after_sync();
+      if (leader) {
+        issue_s<D>(tm_s, tmem + kColK, ds.q_kmaj((it + 2) % C::kStages));
+        umma_commit(sy.s_full(b));
+      }
+      __syncwarp();
+    }
   }
   // Completes when every product issued above has: the epilogue's signal,
   // and the condition for releasing tensor memory.
@@ -346,7 +405,33 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint64_t qk2 = f2_pack(p.qk_scale, p.qk_scale);
   bool ok = true;
-  for (int it = 0; it < n; ++it) {
+  {
+    // K of this thread's key row into tensor memory, the A operand of S^T:
+    // row r of the 128-byte-swizzled K tile (16-byte chunk c of a 64-column
+    // slab at chunk c ^ (r % 8)), two bf16 values of d per column.
+    ok = __all_sync(0xffffffffu, wait_phase(sy.kv_full, 0, sy, p, kSiteDs));
+    if (ok) {
+#pragma unroll
+      for (int sl = 0; sl < D / 64; ++sl) {
+        uint32_t kw[32];
+        const uint8_t* krow = smem + C::kKOff + sl * C::kKSlab + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(krow + ((c ^ (r & 7)) * 16));
+          kw[4 * c] = v.x;
+          kw[4 * c + 1] = v.y;
+          kw[4 * c + 2] = v.z;
+          kw[4 * c + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kColK + sl * 32, kw);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sy.k_ready);
+    }
+  }
+  for (int it = 0; it < n && ok; ++it) {
     const int b = it & 1;
     const int st = it % C::kStages;
     const int q0 = (j0 + it) * kBlockQ;
@@ -399,11 +484,15 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
     // tile in shared memory (the B operand of dQ^T; 16-byte chunk ch of row r
     // at chunk ch ^ (r % 8)).
     w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
-    if (it >= 2) w = w && wait_phase(sy.ds_free(b), ((it >> 1) - 1) & 1, sy, p, kSiteDs);
+    // The dS^T tile in shared memory was last read by dQ^T(it-1): wait for
+    // dq_full's completion of step it-1.  (A parity wait sees its phase only
+    // while the barrier is at most one completion past it; the completion of
+    // step it needs this warpgroup's step it, so it cannot have happened.)
+    if (it >= 1) w = w && wait_phase(sy.dq_full, (it - 1) & 1, sy, p, kSiteDs);
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after_sync();
-    uint8_t* ds_row = smem + C::kDsOff + b * C::kDsBytes + r * 128;
+    uint8_t* ds_row = smem + C::kDsOff + r * 128;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t d32[32];
@@ -516,10 +605,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
               const BwdParams p) {
   using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  if ((sbase & 1023u) != 0) {  // the whole CTA leaves before any barrier
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteAlign);
+    return;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int kb = blockIdx.x;
@@ -534,6 +625,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint32_t b = sbase + C::kBarOff;
     auto next = [&]() { const uint32_t r = b; b += 8; return r; };
     sy.kv_full = next();
+    sy.k_ready = next();
     sy.stage_full0 = next();
     for (int i = 1; i < C::kStages; ++i) next();
     sy.stage_empty0 = next();
@@ -544,8 +636,6 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     sy.sm_done = next();
     sy.dq_full = next();
     sy.dq_free = next();
-    sy.ds_free0 = next();
-    next();
     sy.acc_done = next();
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
@@ -553,14 +643,12 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   if (threadIdx.x == 0) {
     mbar_init(sy.kv_full, 1);
+    mbar_init(sy.k_ready, 4);  // one arrival per P / dS warp
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(sy.stage_full(i), 1);
       mbar_init(sy.stage_empty(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(sy.s_full(i), 1);
-      mbar_init(sy.ds_free(i), 1);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(sy.s_full(i), 1);
     mbar_init(sy.dp_full, 1);
     mbar_init(sy.sm_done, 4);  // one arrival per P / dS warp
     mbar_init(sy.dq_full, 1);

@@ -117,6 +117,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return p;
 }
 
+// Brings the box of a 3-D tiled copy at the given coordinates into L2 (no
+// shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // 3-D tiled store from shared memory; rows outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src,
                                              int32_t c0, int32_t c1, int32_t c2) {
