@@ -37,6 +37,10 @@ KERNEL_SOURCES = [
     os.path.join(ROOT, "exact_attention_20_gb300", "csrc", n)
     for n in ("fa_fwd_kernel.cuh", "sm103_ptx.cuh", "fa_api.cu")
 ]
+BWD_KERNEL_SOURCES = [
+    os.path.join(ROOT, "exact_attention_20_gb300", "csrc", n)
+    for n in ("fa_bwd_kernel.cuh", "sm103_ptx.cuh", "fa_bwd.cu")
+]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FLUSH_BYTES = 256 << 20
 
@@ -46,9 +50,9 @@ def flops(w, causal):
     return f / 2 if causal else f
 
 
-def kernel_hash():
+def kernel_hash(sources=None):
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources or KERNEL_SOURCES:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -71,6 +75,17 @@ def recorded_traffic(workload, causal):
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("bytes_per_launch", {}).get(f"{workload}:{'causal' if causal else 'non-causal'}")
+
+
+def recorded_bwd_traffic(workload, causal):
+    """The same for fa_bwd_kernel (its own sources and record)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f).get("backward", {})
+    if d.get("kernel_hash") != kernel_hash(BWD_KERNEL_SOURCES):
         return None
     return d.get("bytes_per_launch", {}).get(f"{workload}:{'causal' if causal else 'non-causal'}")
 
@@ -477,7 +492,8 @@ def run_backward(args):
         "per_mask": per_mask,
         "roofline": {"bound": "tensor", "achieved": per_mask[dom]["tflops"], "peak": peak, "unit": "TFLOP/s",
                      "frac": per_mask[dom]["frac_of_measured_peak"], "peak_kind": f"{peak_src} bf16 dense, burst",
-                     "timed_span": "one fa_bwd call: prep, fa_bwd_kernel, dQ conversion", "mask": dom},
+                     "timed_span": "one fa_bwd call: prep, fa_bwd_kernel, dQ conversion", "mask": dom,
+                     "kernel": "fa_bwd_kernel", "traffic": recorded_bwd_traffic(w.name, dom == "causal")},
         "gpu_launches": args.steps * len(per_mask) * fa.BWD_KERNELS_PER_CALL,
         "clocks": clocks}), flush=True)
 
