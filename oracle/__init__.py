@@ -13,6 +13,7 @@ from .attention import (  # noqa: F401
     softmax_safe,
     tiled_attention,
 )
+from . import fp8  # noqa: F401
 from .attention_backward import (  # noqa: F401
     attention_backward,
     rowdot,
