@@ -27,7 +27,7 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;
-  bool attr_set[2][2] = {{false, false}, {false, false}};
+  bool attr_set[2][2][2] = {};  // [FP8 path][d == 128][causal]
   // Workspace for the parts of split items, one per stream so that calls on
   // different streams never share it.  Allocated on a stream's first call.
   std::vector<std::pair<cudaStream_t, float*>> workspaces;
@@ -233,21 +233,39 @@ float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
   return ptr;
 }
 
-template <int D, bool CAUSAL>
+// The FP8 path's per-block scales (all null on the bf16 path).
+struct Fp8Scales {
+  const float* q = nullptr;
+  const float* k = nullptr;
+  const float* v = nullptr;
+};
+
+template <int D, bool CAUSAL, int E = 2>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk,
            float scale, cudaStream_t stream, DeviceInfo* di, unsigned long long wait_limit_ns,
-           int starve_kv, int max_ctas, const fa_internal::Scratch& fixed) {
-  using C = fa::Cfg<D>;
+           int starve_kv, int max_ctas, const fa_internal::Scratch& fixed, const Fp8Scales& sc = {}) {
+  using C = fa::Cfg<D, E>;
   CUtensorMap tq, tk, tv;
-  if (!fa::encode_bf16_3d(&tq, q, D, Nq, BH, 64, fa::kBlockM) ||
-      !fa::encode_bf16_3d(&tk, k, D, Nk, BH, 64, fa::kBlockN) ||
-      !fa::encode_bf16_3d(&tv, v, D, Nk, BH, 64, fa::kBlockN))
-    return FA_ERR_LAUNCH;
+  if constexpr (E == 2) {
+    if (!fa::encode_bf16_3d(&tq, q, D, Nq, BH, 64, fa::kBlockM) ||
+        !fa::encode_bf16_3d(&tk, k, D, Nk, BH, 64, fa::kBlockN) ||
+        !fa::encode_bf16_3d(&tv, v, D, Nk, BH, 64, fa::kBlockN))
+      return FA_ERR_LAUNCH;
+  } else {
+    // e4m3 codes: Q [BH][Nq][D] and K [BH][Nk][D] in 128-row boxes of one
+    // 128-byte row each; V transposed, [BH][D][Nk_pad], in boxes of D rows of
+    // 128 keys
+    const uint64_t nk_pad = (static_cast<uint64_t>(Nk) + fa::kBlockN - 1) / fa::kBlockN * fa::kBlockN;
+    if (!fa::encode_u8_3d(&tq, q, D, Nq, BH, 128, fa::kBlockM) ||
+        !fa::encode_u8_3d(&tk, k, D, Nk, BH, 128, fa::kBlockN) ||
+        !fa::encode_u8_3d(&tv, v, nk_pad, D, BH, fa::kBlockN, D))
+      return FA_ERR_LAUNCH;
+  }
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    bool& set = di->attr_set[D == 128][CAUSAL];
+    bool& set = di->attr_set[E == 1][D == 128][CAUSAL];
     if (!set) {
-      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL>,
+      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, E>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::kSmemBytes) != cudaSuccess)
         return FA_ERR_LAUNCH;
@@ -269,6 +287,9 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit_ns = wait_limit_ns;
   p.starve_kv = starve_kv;
+  p.q_scale = sc.q;
+  p.k_scale = sc.k;
+  p.v_scale = sc.v;
   p.part_o = nullptr;
   p.part_lse = nullptr;
   const PlanShape shape{Nq, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
@@ -291,7 +312,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     p.part_lse = ws + ws_slots(di) * fa::kItemRows * 128;
     p.counters = reinterpret_cast<int*>(ws + ws_counter_offset(di));
   }
-  fa::fa_fwd_kernel<D, CAUSAL><<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  fa::fa_fwd_kernel<D, CAUSAL, E><<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }
@@ -353,6 +374,42 @@ int fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse
                 int Nq, int Nk, int d, int causal, float scale, void* stream) {
   return dispatch(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, static_cast<cudaStream_t>(stream),
                   kWaitLimitNs, 0, 0, fa_internal::Scratch{});
+}
+
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int N, int d, int causal, float scale,
+               void* stream) {
+  if (B < 1 || H < 1 || N < 1 || d != 128 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_pad = (static_cast<long long>(N) + fa::kBlockN - 1) / fa::kBlockN * fa::kBlockN;
+  if (BH * n_pad * d >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (!q8 || !k8 || !vt8 || !q_scale || !k_scale || !v_scale || !o || !lse) return FA_ERR_NULL;
+  auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+  if (mis(q8, 16) || mis(k8, 16) || mis(vt8, 16) || mis(o, 16)) return FA_ERR_ALIGN;
+  if (mis(q_scale, 4) || mis(k_scale, 4) || mis(v_scale, 4) || mis(lse, 4)) return FA_ERR_ALIGN;
+  const size_t nblk = static_cast<size_t>(n_pad / fa::kBlockN);
+  const size_t ob = static_cast<size_t>(BH) * N * d * 2, lb = static_cast<size_t>(BH) * N * 4;
+  const void* ins[6] = {q8, k8, vt8, q_scale, k_scale, v_scale};
+  const size_t in_bytes[6] = {static_cast<size_t>(BH) * N * d, static_cast<size_t>(BH) * N * d,
+                              static_cast<size_t>(BH) * d * n_pad, BH * nblk * 4, BH * nblk * 4,
+                              static_cast<size_t>(BH) * 4};
+  for (int i = 0; i < 6; ++i)
+    if (overlaps(o, ob, ins[i], in_bytes[i]) || overlaps(lse, lb, ins[i], in_bytes[i])) return FA_ERR_ALIAS;
+  if (overlaps(o, ob, lse, lb)) return FA_ERR_ALIAS;
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (di == nullptr) return FA_ERR_LAUNCH;
+  if (!di->supported) return FA_ERR_DEVICE;
+  Fp8Scales sc;
+  sc.q = q_scale;
+  sc.k = k_scale;
+  sc.v = v_scale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return causal ? launch<128, true, 1>(q8, k8, vt8, o, lse, static_cast<int>(BH), N, N, scale, s, di, kWaitLimitNs,
+                                       0, 0, fa_internal::Scratch{}, sc)
+                : launch<128, false, 1>(q8, k8, vt8, o, lse, static_cast<int>(BH), N, N, scale, s, di,
+                                        kWaitLimitNs, 0, 0, fa_internal::Scratch{}, sc);
 }
 
 const char* fa_strerror(int code) {

@@ -58,11 +58,17 @@ constexpr int kSiteProducer = 1;
 constexpr int kSiteMma = 2;
 constexpr int kSiteSoftmax = 3;
 
-template <int D>
+// E is the operand size in bytes: 2 for bf16, 1 for the FP8 (e4m3) path.
+// A slab is 128 rows of 128 bytes (64 bf16 or 128 e4m3 values), one TMA box.
+template <int D, int E = 2>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  static constexpr int kTileBytes = (D / 64) * kSlabBytes;         // one 128 x D bf16 tile
-  static constexpr int kStages = (D == 128) ? 5 : 9;               // K/V ring depth (tiles)
+  static_assert(E == 2 || (E == 1 && D == 128), "the FP8 path takes d = 128");
+  static constexpr int kSlabs = D * E / 128;                       // slabs per 128 x D tile
+  static constexpr int kTileBytes = kSlabs * kSlabBytes;           // one 128 x D tile
+  static constexpr int kStages = kTileBytes == 2 * kSlabBytes ? 5 : 9;  // K/V ring depth (tiles)
+  static constexpr int kQkInstr = D * E / 32;                      // S = Q K^T: 32 bytes of K each
+  static constexpr int kPvInstr = kBlockN * E / 32;                // O += P V: likewise
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQOff + kQTiles * kTileBytes;
   static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
@@ -114,6 +120,9 @@ struct FwdParams {
   float qk_scale;          // scale * log2(e)
   unsigned long long wait_limit_ns;
   int starve_kv;           // watchdog self-test: the producer never delivers K/V
+  const float* q_scale;    // FP8 path: [BH][ceil(Nq / 128)], one per 128 query rows
+  const float* k_scale;    // FP8 path: [BH][ceil(Nk / 128)], one per 128 keys
+  const float* v_scale;    // FP8 path: [BH], one per head
   int* counters;           // workspace: per (split item, query tile, warp quadrant) part arrivals (0 between launches)
   WorkRange range[kMaxCtas];
   SlotPair slots[kMaxCtas];
@@ -227,10 +236,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int E = 2>
 __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              uint32_t sbase, const Sync& sy, const FwdParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E>;
   uint32_t q_loads[2] = {0, 0};
   uint32_t kv_count = 0;
   const uint64_t pol_q = l2_policy_evict_first();
@@ -266,8 +275,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
       const uint32_t dst = sbase + C::kQOff + t * C::kTileBytes;
       const int row = rb * kItemRows + t * kBlockM;
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * 64, row, bh, pol_q);
+      for (int s = 0; s < C::kSlabs; ++s)
+        tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * (128 / E), row, bh, pol_q);
     }
     if (p.starve_kv) continue;  // self-test: never deliver K/V
     for (int j = ch.kb; j < ch.ke && ok; ++j) {
@@ -281,9 +290,15 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
         mbar_arrive_expect_tx(full, C::kTileBytes);
         const uint32_t dst = sbase + C::kKVOff + slot * C::kTileBytes;
         const CUtensorMap* map = which == 0 ? tmK : tmV;
+        if (E == 1 && which == 1) {
+          // the FP8 path's V is stored transposed, [BH][D][keys]: the tile is
+          // D rows of 128 keys
+          tma_load_3d_hint(dst, map, full, j * kBlockN, 0, bh, pol_kv);
+        } else {
 #pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_3d_hint(dst + s * kSlabBytes, map, full, s * 64, j * kBlockN, bh, pol_kv);
+          for (int s = 0; s < C::kSlabs; ++s)
+            tma_load_3d_hint(dst + s * kSlabBytes, map, full, s * (128 / E), j * kBlockN, bh, pol_kv);
+        }
         ++kv_count;
       }
     }
@@ -337,10 +352,10 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 // tile 0's group, tile 1's group, tile 0's next group, ...  Each tile's
 // instructions stay in one thread, in issue order, so P_t(j-1) is read before
 // S_t(j) overwrites the same tensor-memory columns.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int E = 2>
 __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, const Sync& sy,
                                         const FwdParams& p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E>;
   const uint32_t bar_q_full = t ? sy.q_full[1] : sy.q_full[0];
   const uint32_t bar_q_empty = t ? sy.q_empty[1] : sy.q_empty[0];
   const uint32_t bar_s_full = t ? sy.s_full[1] : sy.s_full[0];
@@ -354,7 +369,10 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
   // cycles, faster than a descriptor can be assembled from scratch).
   const uint64_t q_desc = sdesc_advance(sdesc_sw128(sbase + C::kQOff, 16, 1024), t * C::kTileBytes);
   const uint64_t k_desc0 = sdesc_sw128(sbase + C::kKVOff, 16, 1024);
-  const uint64_t v_desc0 = sdesc_sw128(sbase + C::kKVOff, kSlabBytes, 1024);
+  // bf16: V [keys][d], an MN-major operand, slabs of d 16 KB apart; FP8:
+  // V^T [d][keys], a K-major operand like K
+  const uint64_t v_desc0 =
+      E == 2 ? sdesc_sw128(sbase + C::kKVOff, kSlabBytes, 1024) : sdesc_sw128(sbase + C::kKVOff, 16, 1024);
   const uint32_t tm_s = tmem + t * 128;
   const uint32_t tm_o = tmem + 256 + t * 128;
   uint32_t q_uses = 0, kv_count = 0, pr_par = 0, of_par = 1, turn_par = 0;
@@ -410,14 +428,16 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       if (do_s) wait_full(ck);
       // Every operand of the group is computed before the turn is taken, so
       // that the turn holds only the MMA instructions themselves.
-      uint64_t dv[kBlockN / 16], dq[D / 16], dk[D / 16];
+      uint64_t dv[C::kPvInstr], dq[C::kQkInstr], dk[C::kQkInstr];
       {
         const uint64_t v0 = sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes);
         const uint64_t k0 = sdesc_advance(k_desc0, (ck % C::kStages) * C::kTileBytes);
+        // P.V: bf16 takes 16 keys (two 8-row groups, 2048 bytes) of the
+        // MN-major V per instruction, FP8 32 keys (32 bytes) of the K-major V^T
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) dv[kk] = sdesc_advance(v0, kk * 2048);
+        for (int kk = 0; kk < C::kPvInstr; ++kk) dv[kk] = sdesc_advance(v0, E == 2 ? kk * 2048 : kk * 32);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kQkInstr; ++kk) {
           const uint32_t off = (kk / 4) * kSlabBytes + (kk % 4) * 32;
           dq[kk] = sdesc_advance(q_desc, off);
           dk[kk] = sdesc_advance(k0, off);
@@ -429,16 +449,30 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {
+      // A = P from tensor memory: 8 columns per instruction either way (16
+      // bf16 or 32 e4m3 values of each row)
       if (do_pv) {
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
+        if constexpr (E == 2) {
+          constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, D, /*b_mn_major=*/true);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(tm_o, tm_s + kk * 8, dv[kk], idesc_pv, kk > 0 ? 1u : acc0);
+          for (int kk = 0; kk < C::kPvInstr; ++kk) umma_ts(tm_o, tm_s + kk * 8, dv[kk], idesc_pv, kk > 0 ? 1u : acc0);
+        } else {
+          constexpr uint32_t idesc_pv = idesc_e4m3_f32(kBlockM, D, /*b_mn_major=*/false);
+#pragma unroll
+          for (int kk = 0; kk < C::kPvInstr; ++kk)
+            umma_ts_f8(tm_o, tm_s + kk * 8, dv[kk], idesc_pv, kk > 0 ? 1u : acc0);
+        }
       }
       if (do_s) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
+        if constexpr (E == 2) {
+          constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_ss(tm_s, dq[kk], dk[kk], idesc_qk, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::kQkInstr; ++kk) umma_ss(tm_s, dq[kk], dk[kk], idesc_qk, kk > 0 ? 1u : 0u);
+        } else {
+          constexpr uint32_t idesc_qk = idesc_e4m3_f32(kBlockM, kBlockN, /*b_mn_major=*/false);
+#pragma unroll
+          for (int kk = 0; kk < C::kQkInstr; ++kk) umma_ss_f8(tm_s, dq[kk], dk[kk], idesc_qk, kk > 0 ? 1u : 0u);
+        }
       }
       // The commits come after both products so that the two run back to
       // back, and before the hand-over so that they cannot be queued behind
@@ -648,7 +682,7 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
 // ---------------------------------------------------------------------------
 // Softmax / correction / epilogue warpgroup (128 threads, one row each)
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int E = 2>
 __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParams& p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -657,7 +691,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * 128;
   const uint32_t tO = tmem + lane_off + 256 + t * 128;
-  const float qk = p.qk_scale;
+  const float qk_base = p.qk_scale;
   const bool ragged = (p.Nk % kBlockN) != 0;
   // this warpgroup's barriers, selected once (no run-time array indexing)
   const uint32_t bar_s_full = t ? sy.s_full[1] : sy.s_full[0];
@@ -681,6 +715,10 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     const int n = tiles_for<CAUSAL>(rb, t, p);       // key tiles of this query tile in the item
     const int ne = min(ch.ke, n);                    // ... and its part in this chunk: [kb, ne)
     const int row = rb * kItemRows + t * kBlockM + row_in_tile;
+    // FP8 path: this query tile's scale (one per 128 query rows)
+    const float sq = E == 1 ? p.q_scale[static_cast<size_t>(bh) * ((p.Nq + kBlockM - 1) / kBlockM) +
+                                        rb * kQTiles + t]
+                            : 1.f;
     if (ne <= ch.kb) {
       // No key tile of this query tile lies in the chunk (past its diagonal).
       // A part still reports its rows, as an empty part: LSE = -inf.
@@ -701,6 +739,9 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     float lq = 0.f;       // the same terms rounded to bf16 (what P.V multiplies), for O
 
     for (int j = ch.kb; j < ne; ++j) {
+      // the factor from the tensor core's sums to log2-units scores: the
+      // softmax scale times log2 e, and on the FP8 path the Q and K tiles' scales
+      const float qk = E == 1 ? qk_base * sq * p.k_scale[static_cast<size_t>(bh) * p.n_key_tiles + j] : qk_base;
       ok = wait_phase(bar_s_full, s_par, sy, p, kSiteSoftmax);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -733,23 +774,49 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t pk[16];
+          if constexpr (E == 2) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = c4 * 32 + 2 * i;
-            const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
-            float xa, xb;
-            f2_unpack(x, xa, xb);
-            const float a = ex2_approx(xa);
-            const float b = ex2_approx(xb);
-            pk[i] = pack_bf16x2(a, b);
-            sum2 = f2_add(sum2, f2_pack(a, b));
-            // also sum the bf16 values the P.V product multiplies, so that
-            // O / lq is an exact weighted average of the value rows
-            add_bf16x2_halves(lqs[(i & 1) * 2], lqs[(i & 1) * 2 + 1], pk[i]);
-            if (with_max) mx[c4] = fmax3(mx[c4], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            for (int i = 0; i < 16; ++i) {
+              const int c = c4 * 32 + 2 * i;
+              const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
+              float xa, xb;
+              f2_unpack(x, xa, xb);
+              const float a = ex2_approx(xa);
+              const float b = ex2_approx(xb);
+              pk[i] = pack_bf16x2(a, b);
+              sum2 = f2_add(sum2, f2_pack(a, b));
+              // also sum the bf16 values the P.V product multiplies, so that
+              // O / lq is an exact weighted average of the value rows
+              add_bf16x2_halves(lqs[(i & 1) * 2], lqs[(i & 1) * 2 + 1], pk[i]);
+              if (with_max) mx[c4] = fmax3(mx[c4], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            }
+            tmem_st16(tS + c4 * 16, pk);
+          } else {
+            // FP8 path: P rounded to e4m3, four per 32-bit column
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int c = c4 * 32 + 4 * i;
+              const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), qk2, negm2);
+              const uint64_t x23 =
+                  f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), qk2, negm2);
+              float x0, x1, x2, x3;
+              f2_unpack(x01, x0, x1);
+              f2_unpack(x23, x2, x3);
+              const float a = ex2_approx(x0), b = ex2_approx(x1), cc = ex2_approx(x2), dd = ex2_approx(x3);
+              pk[i] = pack_e4m3x4(a, b, cc, dd);
+              sum2 = f2_add(sum2, f2_add(f2_pack(a, b), f2_pack(cc, dd)));
+              // the e4m3 values the P.V product multiplies, summed for lq
+              add_e4m3x2_halves(lqs[0], lqs[1], static_cast<uint16_t>(pk[i] & 0xffffu));
+              add_e4m3x2_halves(lqs[2], lqs[3], static_cast<uint16_t>(pk[i] >> 16));
+              if (with_max) {
+                mx[c4] = fmax3(mx[c4], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+                mx[c4] = fmax3(mx[c4], __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+              }
+            }
+            tmem_st8(tS + c4 * 8, pk);
           }
-          tmem_st16(tS + c4 * 16, pk);
         }
         f2_unpack(sum2, sa, sb);
         lq_tile = (lqs[0] + lqs[1]) + (lqs[2] + lqs[3]);
@@ -851,7 +918,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     tc_fence_after_sync();
-    const float inv_l = 1.f / lq;
+    // FP8 path: V's per-head scale comes in here (it is common to every key)
+    const float inv_l = (E == 1 ? p.v_scale[bh] : 1.f) / lq;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
     const float lse_row = (m_ref + log2f(l)) * 0.69314718055994531f;
     if (ch.slot < 0) {
@@ -914,11 +982,11 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
 // ---------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int E = 2>
 __global__ void __launch_bounds__(kNumThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, E>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -988,15 +1056,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp >= 8) {
     setmaxnreg_dec<kRegsAux>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer<D, CAUSAL>(&tmQ, &tmK, &tmV, sbase, sy, p);
+      if (lane == 0) run_producer<D, CAUSAL, E>(&tmQ, &tmK, &tmV, sbase, sy, p);
       __syncwarp();
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      run_mma<D, CAUSAL>(warp - kMmaWarp, sbase, tmem, sy, p);
+      run_mma<D, CAUSAL, E>(warp - kMmaWarp, sbase, tmem, sy, p);
       __syncwarp();
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
-    run_softmax<D, CAUSAL>(warp >> 2, tmem, sy, p);
+    run_softmax<D, CAUSAL, E>(warp >> 2, tmem, sy, p);
   }
 
   tc_fence_before_sync();

@@ -278,6 +278,34 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0
+// in bits 7-9 and 10-12) and an fp32 accumulator; the other fields as for
+// kind::f16.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// The kind::f8f6f4 forms of umma_ss and umma_ts (32 values of K per instruction).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -357,6 +385,12 @@ __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t* r) {
 
 #define FA_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr),
+               FA_W8(0)
+               : "memory");
+}
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -447,6 +481,27 @@ __device__ __forceinline__ void add_bf16x2_halves(float& acc_lo, float& acc_hi, 
       "add.rn.f32.bf16 %1, hi, %1;\n\t}"
       : "+f"(acc_lo), "+f"(acc_hi)
       : "r"(pk));
+}
+
+// Four fp32 values to e4m3 (round to nearest even, saturating), packed
+// little end first: a in bits 0-7, ..., d in bits 24-31.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// acc_lo += the e4m3 value in bits 0-7 of h2, acc_hi += the one in bits 8-15
+// (each widened exactly, through f16, and added in fp32).
+__device__ __forceinline__ void add_e4m3x2_halves(float& acc_lo, float& acc_hi, uint16_t h2) {
+  asm("{\n\t.reg .b32 f2;\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.f16x2.e4m3x2 f2, %2;\n\t"
+      "mov.b32 {lo, hi}, f2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\t"
+      "add.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "h"(h2));
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

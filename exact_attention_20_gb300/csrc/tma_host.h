@@ -43,6 +43,23 @@ inline bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, ui
   return r == CUDA_SUCCESS;
 }
 
+// A one-byte tensor (the FP8 path's e4m3 codes) viewed as
+// [planes][rows][cols] (cols contiguous), in boxes of box_cols x box_rows x 1
+// with 128-byte swizzling; rows outside the tensor read as zero.
+inline bool encode_u8_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t planes, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols, cols * rows};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // An fp32 tensor viewed as [planes][rows][cols] (cols contiguous), in boxes
 // of box_cols x box_rows x 1 without swizzling (the box is plain row-major in
 // shared memory).  Used for reductions into it: elements outside the tensor

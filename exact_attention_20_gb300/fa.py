@@ -35,6 +35,8 @@ SIGNATURES = {
     "fa_fwd_plan": (_I, [_I, _I, _I, _I, _I, _I, _P, _P]),
     "fa_fwd_rect": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "fa_quantize_fp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
     "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
@@ -214,6 +216,68 @@ def attention_backward(q, k, v, o, lse, do, causal: bool = False, scale: float |
     dv = torch.empty_like(v)
     fa_bwd(q, k, v, o, lse, do, dq, dk, dv, causal=causal, scale=scale, stream=stream)
     return dq, dk, dv
+
+
+def quantize_fp8(x, mode: int, stream=None):
+    """bf16 x [B, H, N, d] to e4m3 codes (uint8) and fp32 scales.
+
+    mode 0 (Q, K): codes [B, H, N, d], scales [B, H, ceil(N/128)], one per 128 rows.
+    mode 1 (V): codes transposed [B, H, d, ceil(N/128)*128] (padding keys 0),
+    scales [B, H], one per head.
+    """
+    if x.dim() != 4 or x.dtype != torch.bfloat16 or not x.is_contiguous() or x.device.type != "cuda":
+        raise ValueError("x must be a contiguous bf16 CUDA tensor [B, H, N, d]")
+    B, H, N, d = x.shape
+    nblk = (N + 127) // 128
+    if mode == 0:
+        x8 = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H, nblk), dtype=torch.float32, device=x.device)
+    elif mode == 1:
+        x8 = torch.empty((B, H, d, nblk * 128), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    else:
+        raise ValueError("mode is 0 (Q, K) or 1 (V)")
+    with torch.cuda.device(x.device):
+        rc = lib().fa_quantize_fp8(x.data_ptr(), x8.data_ptr(), scales.data_ptr(), B, H, N, d, mode,
+                                   _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return x8, scales
+
+
+def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, causal: bool = False,
+               scale: float | None = None, stream=None) -> None:
+    """The forward on FP8 operands (the layouts of quantize_fp8), into caller-owned O and LSE."""
+    B, H, N, d = q8.shape
+    dev = q8.device
+    nblk = (N + 127) // 128
+    _check("q8", q8, torch.uint8, (B, H, N, d), dev)
+    _check("k8", k8, torch.uint8, (B, H, N, d), dev)
+    _check("vt8", vt8, torch.uint8, (B, H, d, nblk * 128), dev)
+    _check("q_scale", q_scale, torch.float32, (B, H, nblk), dev)
+    _check("k_scale", k_scale, torch.float32, (B, H, nblk), dev)
+    _check("v_scale", v_scale, torch.float32, (B, H), dev)
+    _check("o", o, torch.bfloat16, (B, H, N, d), dev)
+    _check("lse", lse, torch.float32, (B, H, N), dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(dev):
+        rc = lib().fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_scale.data_ptr(),
+                              k_scale.data_ptr(), v_scale.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
+                              N, d, int(bool(causal)), float(scale), _stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
+
+
+def attention_fp8(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Quantises bf16 q, k, v to FP8 and runs the FP8 forward; returns (O, LSE)."""
+    q8, sq = quantize_fp8(q, 0, stream)
+    k8, sk = quantize_fp8(k, 0, stream)
+    vt8, sv = quantize_fp8(v, 1, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(q8, k8, vt8, sq, sk, sv, o, lse, causal=causal, scale=scale, stream=stream)
+    return o, lse
 
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):

@@ -197,6 +197,44 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            const void* dout, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
            int causal, float scale, void* stream);
 
+/*
+ * fa_quantize_fp8 — bf16 to FP8 (e4m3) codes with per-block fp32 scales, in
+ * the layouts fa_fwd_fp8 reads.  A block of rows shares one scale
+ * s = amax / 448 (s = 1 for an all-zero block); each element becomes the
+ * e4m3 value nearest to x / s (ties to even, saturating at +-448; the
+ * division in fp32).  The pages name FP8 with per-block scaling
+ * ("FlashAttention and kernels.", section "FlashAttention-2, -3, and what
+ * came after") without fixing the blocks; the reading here:
+ *
+ *   mode 0 (Q, K): x bf16 [B][H][N][d] -> x8 [B][H][N][d] (one byte each),
+ *                  scales [B][H][ceil(N/128)], one per 128 rows;
+ *   mode 1 (V):    x bf16 [B][H][N][d] -> x8 [B][H][d][N_pad], transposed,
+ *                  N_pad = ceil(N/128)*128, keys past N zero;
+ *                  scales [B][H], one per head (V's scale has to factor out
+ *                  of the sum over key tiles).
+ *
+ *   d: 64 or 128.  x, x8 16-byte aligned, scales 4-byte aligned, device
+ *   pointers, no overlaps.  Four launches on `stream` (the scales are
+ *   zeroed, then amax, codes, scales).  Returns FA_OK or a negative fa_status.
+ */
+int fa_quantize_fp8(const void* x, void* x8, float* scales, int B, int H, int N, int d, int mode,
+                    void* stream);
+
+/*
+ * fa_fwd_fp8 — the forward on FP8 operands: O and LSE (as fa_fwd) of
+ * attention on the dequantised inputs q8 * sQ, k8 * sK, v8 * sV, from the
+ * layouts fa_quantize_fp8 writes (q8, k8 mode 0; vt8 mode 1).  d = 128.
+ * S = Q K^T and O += P V run on the tensor core's e4m3 instruction
+ * (kind::f8f6f4) with fp32 accumulation; P is rounded to e4m3 before P V
+ * (P <= 2^8 by the forward's lazy maximum, inside e4m3's range); the scales
+ * enter the exponent (sQ sK) and the final division (sV).  Same work
+ * division, workspace and errors as fa_fwd; o bf16 [B][H][N][128] and lse
+ * fp32 [B][H][N] must not overlap an input.
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+               const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,
+               int d, int causal, float scale, void* stream);
+
 const char* fa_strerror(int code);
 
 /*

@@ -28,8 +28,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    assert names == ["fa_bwd", "fa_fwd", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
-                     "fa_get_device_status", "fa_strerror", "fa_version", "fa_watchdog_selftest"]
+    assert names == ["fa_bwd", "fa_fwd", "fa_fwd_fp8", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
+                     "fa_get_device_status", "fa_quantize_fp8", "fa_strerror", "fa_version",
+                     "fa_watchdog_selftest"]
 
 
 def test_library_exports_every_declared_symbol(fa):
@@ -212,3 +213,35 @@ def test_bwd_entry_checks_arguments(fa):
     bad = list(args)
     bad[8] = L                                # dv over lse
     assert call(*bad) == fa.FA_ERR_ALIAS
+
+
+def test_fp8_entries_check_arguments(fa):
+    fwd, quant = fa.lib().fa_fwd_fp8, fa.lib().fa_quantize_fp8
+    Q8, K8, V8, SQ, SK, SV = (A + i * STEP for i in range(9, 15))
+    args = [Q8, K8, V8, SQ, SK, SV, O, L]
+
+    def call(*ptrs, B=1, H=2, N=256, d=128, causal=0, scale=0.125):
+        return fwd(*ptrs, B, H, N, d, causal, scale, None)
+
+    assert call(*args, d=64) == fa.FA_ERR_INVALID_ARG      # the FP8 path takes d = 128
+    assert call(*args, N=0) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert call(*args, scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    for i in range(8):
+        bad = list(args)
+        bad[i] = None
+        assert call(*bad) == fa.FA_ERR_NULL, i
+        bad = list(args)
+        bad[i] = args[i] + (2 if i >= 3 and i != 6 else 8)
+        assert call(*bad) == fa.FA_ERR_ALIGN, i
+    bad = list(args)
+    bad[6] = Q8 + 64                                        # o over the codes of q
+    assert call(*bad) == fa.FA_ERR_ALIAS
+    bad = list(args)
+    bad[7] = SV                                             # lse over v's scales
+    assert call(*bad) == fa.FA_ERR_ALIAS
+    assert quant(Q, Q8, SQ, 1, 2, 256, 96, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert quant(Q, Q8, SQ, 1, 2, 256, 128, 2, None) == fa.FA_ERR_INVALID_ARG
+    assert quant(None, Q8, SQ, 1, 2, 256, 128, 0, None) == fa.FA_ERR_NULL
+    assert quant(Q, Q8 + 8, SQ, 1, 2, 256, 128, 0, None) == fa.FA_ERR_ALIGN
+    assert quant(Q, Q + 64, SQ, 1, 2, 256, 128, 0, None) == fa.FA_ERR_ALIAS
