@@ -1,6 +1,6 @@
 /*
- * fa_gb300.h — C ABI of the GB300 (sm_103a) fused exact attention forward
- * and backward.
+ * fa_gb300.h — C ABI of the GB300 (sm_103a) fused exact attention: the
+ * forward (bf16, and on FP8 operands), its backward, and the FP8 quantiser.
  *
  * The operation.  For every batch b, head h and query row i,
  *
@@ -14,7 +14,8 @@
  * and "FlashAttention and kernels." (section "FlashAttention's forward pass").
  * The kernel computes it tile by tile with the online softmax (running row
  * maximum, running row sum, rescaled fp32 accumulator, exp2), so the N x N
- * score matrix never reaches device memory.
+ * score matrix never reaches device memory.  fa_bwd computes the gradients
+ * of O with respect to Q, K and V by the same tiles, rebuilding P from LSE.
  *
  * Conventions shared by every entry point:
  *   - Pointers named q, k, v, o, lse are DEVICE pointers on the current device.
@@ -24,8 +25,10 @@
  *     40 MB on a GB300) plus 2048 counters for the parts of split work
  *     items, allocated (and its counters zeroed) on the
  *     first fa_fwd on that stream that splits an item and kept until the
- *     process exits.  Calls on one stream reuse its workspace in stream
- *     order; calls on different streams never share one.
+ *     process exits; and, per stream, the backward's workspace (see
+ *     fa_bwd).  fa_fwd_noalloc and fa_quantize_fp8 allocate nothing.  Calls
+ *     on one stream reuse its workspaces in stream order; calls on different
+ *     streams never share one.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream) and return a status code.
  *   - Status 0 is FA_OK.  A negative status is returned for an error found
