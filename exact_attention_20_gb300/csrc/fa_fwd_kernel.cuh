@@ -416,18 +416,11 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       const bool do_s = s < ne;
       const uint32_t cv = kv_count + 2 * (s - 1 - kb) + 1;  // V_{s-1}
       const uint32_t ck = kv_count + 2 * (s - kb);          // K_s
-      if (do_pv) {
-        wait_full(cv);
-        wait_voted(bar_p_ready, pr_par);
-        pr_par ^= 1u;
-        if (s == kb + 1) {
-          wait_voted(bar_o_free, of_par);
-          of_par ^= 1u;
-        }
-      }
+      // K/V (landed long before, as a rule) first, then the descriptors, and
+      // the softmax's P last: once P is in, only the turn stands between it
+      // and the products.
+      if (do_pv) wait_full(cv);
       if (do_s) wait_full(ck);
-      // Every operand of the group is computed before the turn is taken, so
-      // that the turn holds only the MMA instructions themselves.
       uint64_t dv[C::kPvInstr], dq[C::kQkInstr], dk[C::kQkInstr];
       {
         const uint64_t v0 = sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes);
@@ -444,6 +437,16 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
         }
       }
       const uint32_t acc0 = s > kb + 1 ? 1u : 0u;
+      if (do_pv) {
+        if (s == kb + 1) {
+          wait_voted(bar_o_free, of_par);
+          of_par ^= 1u;
+        }
+        wait_voted(bar_p_ready, pr_par);
+        pr_par ^= 1u;
+      }
+      // Every operand of the group is computed before the turn is taken, so
+      // that the turn holds only the MMA instructions themselves.
       wait_voted(my_turn, turn_par);
       turn_par ^= 1u;
       if (!ok) break;
@@ -476,10 +479,12 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       }
       // The commits come after both products so that the two run back to
       // back, and before the hand-over so that they cannot be queued behind
-      // the other tile's group.  O_t's completion is then signalled with S_t's,
-      // which is when the softmax first needs it.
+      // the other tile's group.  A group has as few as it can: S_t's
+      // completion also tells the softmax that the P.V of the same group is
+      // done (what a rescale of O needs), and o_done is committed only by the
+      // chunk's last group, the P.V alone, for the epilogue.
       if (do_s) umma_commit(bar_s_full);
-      if (do_pv) umma_commit(bar_o_done);
+      if (do_pv && !do_s) umma_commit(bar_o_done);
       if (do_s && s == ne - 1) umma_commit(bar_q_empty);
       if (do_pv) umma_commit(empty(cv));
       if (do_s) umma_commit(empty(ck));
@@ -699,7 +704,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   const uint32_t bar_o_done = t ? sy.o_done[1] : sy.o_done[0];
   const uint32_t bar_o_free = t ? sy.o_free[1] : sy.o_free[0];
   uint32_t s_par = 0;
-  uint32_t pv_count = 0;  // P.V products of this tile so far (o_done completes once per product)
+  uint32_t od_par = 0;  // o_done completes once per chunk in which this tile has keys
   // split items this warp's rows complete, merged after the last chunk
   PendingMerge pend0{-1, 0, false, false, 0.f, 0.f, 0, 0}, pend1 = pend0;
   bool ok = true;
@@ -877,15 +882,10 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       lq = lq * alpha + lq_tile;
 
       if (j > ch.kb && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O_t holds the sum up to tile j-1; bring it to the new reference
-        // maximum where a row moved it (alpha = 1 elsewhere, exact).  Only
-        // then is P.V(j-1) waited for: that is its o_done phase, numbered
-        // from the P.V count (the next one cannot complete before this
-        // step's P, so the barrier is never two phases ahead).
-        ok = wait_phase(bar_o_done, (pv_count - 1) & 1u, sy, p, kSiteSoftmax);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after_sync();
+        // O_t holds the sum up to tile j-1 (that P.V went out in the same
+        // group as S_t(j), whose completion was just waited for); bring it
+        // to the new reference maximum where a row moved it (alpha = 1
+        // elsewhere, exact).
         {
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
@@ -908,15 +908,15 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p_ready);  // one arrival per warp
-      ++pv_count;  // P.V(j) follows
     }
     if (!ok) break;
 
     // Epilogue: wait for the last P.V, then O = O_acc / l in bf16 and the
     // natural-log logsumexp L = (m + log2 l) * ln 2.
-    ok = wait_phase(bar_o_done, (pv_count - 1) & 1u, sy, p, kSiteSoftmax);
+    ok = wait_phase(bar_o_done, od_par, sy, p, kSiteSoftmax);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
+    od_par ^= 1u;
     tc_fence_after_sync();
     // FP8 path: V's per-head scale comes in here (it is common to every key)
     const float inv_l = (E == 1 ? p.v_scale[bh] : 1.f) / lq;
