@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = [os.path.join(PKG, "csrc", n) for n in ("fa_api.cu", "fa_noalloc.cu", "fa_bwd.cu", "fa_fp8.cu")]
 DEPENDS = SOURCES + [
     os.path.join(PKG, "csrc", n)
-    for n in ("fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "fa_fp8_quant.cuh", "sm103_ptx.cuh", "tma_host.h",
+    for n in ("fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh", "fa_fp8_quant.cuh", "fa_decode.cuh", "sm103_ptx.cuh", "tma_host.h",
               "fa_internal.h")
 ] + [os.path.join(ROOT, "include", "fa_gb300.h")]
 

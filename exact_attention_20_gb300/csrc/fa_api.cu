@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "fa_gb300.h"
+#include "fa_decode.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_internal.h"
 #include "tma_host.h"
@@ -317,6 +318,86 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   return FA_OK;
 }
 
+// Few query rows without the causal mask go to the decode kernels.
+bool takes_decode(int BH, int Nq, int causal) {
+  return causal == 0 && Nq <= fa::decode::kMaxRows && BH <= 65535;
+}
+
+// The decode kernels' key chunks: about eight CTAs per SM (two resident at a
+// time, so four waves and a short tail), every chunk a whole number of
+// rounds (64 keys) and at least four of them, and the chunks' partial
+// results within the workspace's part area.
+struct DecodePlan {
+  int keys_per_chunk;
+  int n_chunks;
+};
+DecodePlan decode_plan(const DeviceInfo* di, int BH, int Nq, int Nk, int d) {
+  constexpr int R = fa::decode::kKeysPerRound;
+  const int target = std::max(1, (8 * di->num_sms + BH - 1) / BH);
+  int kpc = (Nk + target - 1) / target;
+  kpc = std::max(4 * R, (kpc + R - 1) / R * R);
+  int n = (Nk + kpc - 1) / kpc;
+  const size_t cap = ws_counter_offset(di);  // floats before the arrival counters
+  const size_t per_chunk = static_cast<size_t>(BH) * Nq * (d + 1);
+  if (n > 1 && static_cast<size_t>(n) * per_chunk > cap) {
+    const int n_max = static_cast<int>(cap / per_chunk);
+    if (n_max < 2) {
+      n = 1;
+      kpc = (Nk + R - 1) / R * R;
+    } else {
+      kpc = ((Nk + n_max - 1) / n_max + R - 1) / R * R;
+      n = (Nk + kpc - 1) / kpc;
+    }
+  }
+  return DecodePlan{kpc, n};
+}
+
+template <int D>
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Nq, int Nk,
+                  float scale, cudaStream_t stream, DeviceInfo* di) {
+  namespace dc = fa::decode;
+  const DecodePlan plan = decode_plan(di, BH, Nq, Nk, D);
+  dc::Params p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.keys_per_chunk = plan.keys_per_chunk;
+  p.n_chunks = plan.n_chunks;
+  p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (plan.n_chunks > 1) {
+    float* ws = stream_workspace(di, stream);
+    if (ws == nullptr) return FA_ERR_LAUNCH;
+    p.part_o = ws;
+    p.part_lse = ws + static_cast<size_t>(BH) * Nq * plan.n_chunks * D;
+  }
+  p.status = di->status;
+  p.wait_limit_ns = kWaitLimitNs;
+  const dim3 grid(plan.n_chunks, BH);
+  constexpr int smem = dc::smem_bytes<D>();
+  auto run = [&](auto kernel) -> bool {
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return false;
+    }
+    kernel<<<grid, dc::kThreadsAll, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess;
+  };
+  const bool launched = Nq == 1 ? run(dc::partial_kernel<D, 1>)
+                        : Nq == 2 ? run(dc::partial_kernel<D, 2>)
+                                  : run(dc::partial_kernel<D, 4>);
+  if (!launched) return FA_ERR_LAUNCH;
+  if (plan.n_chunks > 1) {
+    dc::merge_kernel<D><<<BH * Nq, D, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
+}
+
 int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
              int Nk, int d, int causal, float scale, cudaStream_t stream,
              unsigned long long wait_limit_ns, int starve_kv, int max_ctas,
@@ -328,6 +409,11 @@ int dispatch(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (di == nullptr) return FA_ERR_LAUNCH;
   if (!di->supported) return FA_ERR_DEVICE;
   const int BH = B * H;
+  // the decode kernels (not for the watchdog self-test, a CTA cap or a
+  // caller's fixed scratch, which are the forward kernel's)
+  if (takes_decode(BH, Nq, causal) && starve_kv == 0 && max_ctas == 0 && fixed.ptr == nullptr)
+    return d == 128 ? launch_decode<128>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di)
+                    : launch_decode<64>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di);
   if (d == 128)
     return causal ? launch<128, true>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed)
                   : launch<128, false>(q, k, v, o, lse, BH, Nq, Nk, scale, stream, di, wait_limit_ns, starve_kv, max_ctas, fixed);
@@ -477,6 +563,14 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
   if (di == nullptr) return FA_ERR_LAUNCH;
   if (!di->supported) return FA_ERR_DEVICE;
   const int BH = B * H;
+  if (takes_decode(BH, Nq, causal)) {
+    // the decode kernels: one CTA per key chunk and (batch, head); the heads'
+    // keys are split when there is more than one chunk
+    const DecodePlan plan = decode_plan(di, BH, Nq, Nk, d);
+    *num_ctas = plan.n_chunks * BH;
+    *num_split_items = plan.n_chunks > 1 ? BH : 0;
+    return FA_OK;
+  }
   const int nkt = (Nk + fa::kBlockN - 1) / fa::kBlockN;
   const int nrb = (Nq + fa::kItemRows - 1) / fa::kItemRows;
   static fa::FwdParams p;
