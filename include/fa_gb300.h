@@ -24,8 +24,9 @@
  *     workspace of 2 x (SMs, at most 256) x 256 x 129 fp32 values (about
  *     40 MB on a GB300) plus 2048 counters for the parts of split work
  *     items, allocated (and its counters zeroed) on the
- *     first fa_fwd on that stream that splits an item and kept until the
- *     process exits; and, per stream, the backward's workspace (see
+ *     first fa_fwd on that stream that splits an item (or splits the keys
+ *     of a decode call, whose chunk partials use its first part) and kept
+ *     until the process exits; and, per stream, the backward's workspace (see
  *     fa_bwd).  fa_fwd_noalloc and fa_quantize_fp8 allocate nothing.  Calls
  *     on one stream reuse its workspaces in stream order; calls on different
  *     streams never share one.
@@ -77,8 +78,9 @@ enum fa_status {
  * writing O normalised over its own keys and its logsumexp to the stream's
  * workspace; the CTA whose arrival completes an item's parts merges them
  * (O = sum_r exp(L_r - L) O_r, L = ln sum_r exp(L_r)) after its own work, so
- * a call is always one launch.  Otherwise one CTA takes each item.
- * fa_fwd_plan reports the choice.
+ * such a call is one launch.  Otherwise one CTA takes each item.  Without
+ * the mask and with N <= 4, the call takes the decode kernels instead (see
+ * fa_fwd_rect).  fa_fwd_plan reports the choice.
  *
  * P (the softmax numerators) is rounded to bf16 before the P.V product and O
  * is rounded once to bf16 (round to nearest even) after the fp32 division by
@@ -99,11 +101,20 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *             convention non-square causal attention is checked against in
  *             "How to profile and optimise kernels", Round 4); every row
  *             sees key 0, so no row is ever fully masked.
- * Few query rows over many keys (the decode shape) is the case this opens:
- * when there are no more work items than SMs, the keys of each item are
- * split over several CTAs (at least 16 key tiles each) and the parts merged
- * in the same launch, as for fa_fwd.  Errors as fa_fwd, with Nq and Nk
- * each >= 1 and B*H*Nq*d, B*H*Nk*d < 2^31.
+ * Few query rows over many keys (the decode shape) is the case this opens.
+ *   - causal = 0 and Nq <= 4 (and B*H <= 65535): the decode kernels, on the
+ *     CUDA cores, since the work is bound by reading K and V once.  The keys
+ *     of each (b, h) are cut into equal chunks (about eight CTAs per SM in
+ *     all, each chunk a multiple of 64 keys), each CTA streams its chunk
+ *     through shared memory and writes O normalised over the chunk and its
+ *     logsumexp to the stream's workspace, and a second launch merges the
+ *     chunks (O = sum_c exp(L_c - L) O_c, L = ln sum_c exp(L_c)).  One chunk:
+ *     one launch, written directly.  P stays in fp32 here: nothing is
+ *     rounded before P.V.
+ *   - otherwise the attention kernel of fa_fwd: when there are no more work
+ *     items than SMs, the keys of each item are split over several CTAs (at
+ *     least 16 key tiles each) and the parts merged in the same launch.
+ * Errors as fa_fwd, with Nq and Nk each >= 1 and B*H*Nq*d, B*H*Nk*d < 2^31.
  */
 int fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse,
                 int B, int H, int Nq, int Nk, int d, int causal, float scale, void* stream);
@@ -150,7 +161,9 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  * on the current device for these sizes (no pointer is needed and nothing
  * is launched or allocated):
  * *num_ctas = the attention kernel's grid, *num_split_items = items computed
- * in parts (merged inside the same launch).  The paper has no counterpart;
+ * in parts (merged inside the same launch).  For the decode kernels' shapes:
+ * *num_ctas = chunks x B x H, *num_split_items = B x H when the keys are cut
+ * into more than one chunk (merged by the second launch), else 0.  The paper has no counterpart;
  * it exists so that callers can see how the work is divided.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
  * FA_ERR_INVALID_ARG (sizes as for fa_fwd), FA_ERR_DEVICE or FA_ERR_LAUNCH.
  */
