@@ -29,6 +29,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int* status = nullptr;
   bool attr_set[2][2][2] = {};  // [FP8 path][d == 128][causal]
+  bool decode_attr_set[2][3] = {};  // decode kernels: [d == 128][rows 1, 2, 4]
   // Workspace for the parts of split items, one per stream so that calls on
   // different streams never share it.  Allocated on a stream's first call.
   std::vector<std::pair<cudaStream_t, float*>> workspaces;
@@ -333,7 +334,7 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(const DeviceInfo* di, int BH, int Nq, int Nk, int d) {
   constexpr int R = fa::decode::kKeysPerRound;
-  const int target = std::max(1, (8 * di->num_sms + BH - 1) / BH);
+  const int target = std::min(fa::decode::kMaxChunks, std::max(1, (8 * di->num_sms + BH - 1) / BH));
   int kpc = (Nk + target - 1) / target;
   kpc = std::max(4 * R, (kpc + R - 1) / R * R);
   int n = (Nk + kpc - 1) / kpc;
@@ -378,18 +379,22 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
   p.wait_limit_ns = kWaitLimitNs;
   const dim3 grid(plan.n_chunks, BH);
   constexpr int smem = dc::smem_bytes<D>();
-  auto run = [&](auto kernel) -> bool {
+  auto run = [&](auto kernel, int which) -> bool {
     {
       std::lock_guard<std::mutex> lock(g_mu);
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return false;
+      bool& set = di->decode_attr_set[D == 128][which];
+      if (!set) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+          return false;
+        set = true;
+      }
     }
     kernel<<<grid, dc::kThreadsAll, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess;
   };
-  const bool launched = Nq == 1 ? run(dc::partial_kernel<D, 1>)
-                        : Nq == 2 ? run(dc::partial_kernel<D, 2>)
-                                  : run(dc::partial_kernel<D, 4>);
+  const bool launched = Nq == 1 ? run(dc::partial_kernel<D, 1>, 0)
+                        : Nq == 2 ? run(dc::partial_kernel<D, 2>, 1)
+                                  : run(dc::partial_kernel<D, 4>, 2);
   if (!launched) return FA_ERR_LAUNCH;
   if (plan.n_chunks > 1) {
     dc::merge_kernel<D><<<BH * Nq, D, 0, stream>>>(p);

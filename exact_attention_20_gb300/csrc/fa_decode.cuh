@@ -30,6 +30,7 @@ constexpr int kStages = 3;                    // shared-memory ring depth (round
 constexpr int kGroup = 8;                     // keys a warp loads together
 constexpr int kKeysPerRound = kWarps * kGroup;  // consecutive keys the CTA reads per round
 constexpr int kMaxRows = 4;                   // query rows this path takes
+constexpr int kMaxChunks = 1024;              // key chunks per (batch, head), at most
 
 struct Params {
   const __nv_bfloat16* q;  // [BH][Nq][D]
@@ -310,20 +311,47 @@ __global__ void __launch_bounds__(kThreadsAll, NQ == 4 ? 1 : 2) partial_kernel(c
 }
 
 // One CTA per (batch*head, row): L = log2 sum_c 2^(L_c), O = sum_c 2^(L_c - L) O_c,
-// the largest L_c subtracted first.
+// the largest L_c subtracted first.  The chunks' logsumexps are read once,
+// in parallel, into shared memory; then each thread (one output element)
+// reads its chunks' values eight at a time, so the loads overlap.
 template <int D>
 __global__ void __launch_bounds__(D) merge_kernel(const Params p) {
+  __shared__ float s_w[kMaxChunks];
+  __shared__ float s_red[D / 32];
   const size_t row = blockIdx.x;
   const int e = threadIdx.x;
+  const int n = p.n_chunks;  // <= kMaxChunks (the plan's bound)
   const float* lc = p.part_lse + row * p.n_chunks;
-  float M = -INFINITY;
-  for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, lc[c]);
+  float mx = -INFINITY;
+  for (int c = e; c < n; c += D) {
+    s_w[c] = lc[c];
+    mx = fmaxf(mx, s_w[c]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if ((e & 31) == 0) s_red[e >> 5] = mx;
+  __syncthreads();
+  float M = s_red[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, s_red[w]);
+  for (int c = e; c < n; c += D) s_w[c] = exp2f(s_w[c] - M);
+  __syncthreads();
   float W = 0.f, O = 0.f;
   const float* oc = p.part_o + row * p.n_chunks * D + e;
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const float w = exp2f(lc[c] - M);
-    W += w;
-    O = fmaf(w, oc[static_cast<size_t>(c) * D], O);
+  int c = 0;
+  for (; c + 8 <= n; c += 8) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = oc[static_cast<size_t>(c + i) * D];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      W += s_w[c + i];
+      O = fmaf(s_w[c + i], x[i], O);
+    }
+  }
+  for (; c < n; ++c) {
+    W += s_w[c];
+    O = fmaf(s_w[c], oc[static_cast<size_t>(c) * D], O);
   }
   p.o[row * D + e] = __float2bfloat16_rn(O / W);
   if (e == 0) p.lse[row] = (M + log2f(W)) * 0.69314718055994531f;
