@@ -374,6 +374,9 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
     if (ws == nullptr) return FA_ERR_LAUNCH;
     p.part_o = ws;
     p.part_lse = ws + static_cast<size_t>(BH) * Nq * plan.n_chunks * D;
+    // one arrival counter per (b, h) in the workspace's counters (zero
+    // between launches): the chunks are then merged in the same launch
+    if (BH <= fa::kNumCounters) p.counters = reinterpret_cast<int*>(ws + ws_counter_offset(di));
   }
   p.status = di->status;
   p.wait_limit_ns = kWaitLimitNs;
@@ -396,7 +399,7 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
                         : Nq == 2 ? run(dc::partial_kernel<D, 2>, 1)
                                   : run(dc::partial_kernel<D, 4>, 2);
   if (!launched) return FA_ERR_LAUNCH;
-  if (plan.n_chunks > 1) {
+  if (plan.n_chunks > 1 && p.counters == nullptr) {
     dc::merge_kernel<D><<<BH * Nq, D, 0, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   }

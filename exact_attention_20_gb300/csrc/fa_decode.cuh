@@ -11,8 +11,9 @@
 // output row").  The eight warps' states are combined through shared memory,
 // and the chunks' normalised partial outputs are merged through their
 // logsumexps ("FlashAttention and kernels.", the merge of partial states over
-// key ranges that Flash-Decoding uses).  P stays in fp32: nothing is rounded
-// before P.V.
+// key ranges that Flash-Decoding uses), by the last CTA of each (batch, head)
+// in the same launch or, without arrival counters, by merge_kernel.  P stays
+// in fp32: nothing is rounded before P.V.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,6 +47,8 @@ struct Params {
   float qk_scale;          // softmax scale * log2(e)
   int* status;             // device status word (0 = ok)
   unsigned long long wait_limit_ns;
+  int* counters;           // split, merged in the same launch: [BH] chunk arrivals (0 between launches);
+                           // nullptr: merge_kernel merges afterwards
 };
 
 constexpr int kSiteDecode = 5;  // status code: a decode wait gave up
@@ -308,6 +311,54 @@ __global__ void __launch_bounds__(kThreadsAll, NQ == 4 ? 1 : 2) partial_kernel(c
       if (e == 0) p.lse[row] = lse2 * 0.69314718055994531f;
     }
   }
+  if (!split || p.counters == nullptr) return;
+  // The CTA whose arrival completes this head's chunks merges them, while
+  // the parts are still in L2: L = log2 sum_c 2^(L_c), O = sum_c 2^(L_c - L)
+  // O_c, the largest L_c first.  Every CTA's rows are written (and fenced)
+  // before its arrival is counted; the merging CTA resets the counter.
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(p.counters + bh, 1);
+    s_last = old == p.n_chunks - 1;
+    __threadfence();
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int idx = threadIdx.x; idx < NQ * D; idx += kThreadsAll) {
+    const int r = idx / D, e = idx % D;
+    if (r >= p.Nq) continue;
+    const size_t row = static_cast<size_t>(bh) * p.Nq + r;
+    const float* lc = p.part_lse + row * p.n_chunks;
+    const float* oc = p.part_o + row * p.n_chunks * D + e;
+    float M = -INFINITY;
+    for (int c = 0; c < p.n_chunks; ++c) M = fmaxf(M, __ldcg(lc + c));
+    float W = 0.f, O = 0.f;
+    int c = 0;
+    for (; c + 8 <= p.n_chunks; c += 8) {  // eight chunks' loads in flight together
+      float lv[8], ov[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        lv[i] = __ldcg(lc + c + i);
+        ov[i] = __ldcg(oc + static_cast<size_t>(c + i) * D);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float w = exp2f(lv[i] - M);
+        W += w;
+        O = fmaf(w, ov[i], O);
+      }
+    }
+    for (; c < p.n_chunks; ++c) {
+      const float w = exp2f(__ldcg(lc + c) - M);
+      W += w;
+      O = fmaf(w, __ldcg(oc + static_cast<size_t>(c) * D), O);
+    }
+    p.o[row * D + e] = __float2bfloat16_rn(O / W);
+    if (e == 0) p.lse[row] = (M + log2f(W)) * 0.69314718055994531f;
+  }
+  if (threadIdx.x == 0) p.counters[bh] = 0;
 }
 
 // One CTA per (batch*head, row): L = log2 sum_c 2^(L_c), O = sum_c 2^(L_c - L) O_c,

@@ -107,10 +107,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *     of each (b, h) are cut into equal chunks (about eight CTAs per SM in
  *     all, each chunk a multiple of 64 keys), each CTA streams its chunk
  *     through shared memory and writes O normalised over the chunk and its
- *     logsumexp to the stream's workspace, and a second launch merges the
- *     chunks (O = sum_c exp(L_c - L) O_c, L = ln sum_c exp(L_c)).  One chunk:
- *     one launch, written directly.  P stays in fp32 here: nothing is
- *     rounded before P.V.
+ *     logsumexp to the stream's workspace, and the CTA whose arrival
+ *     completes a (b, h) (one counter per (b, h) among the workspace's
+ *     counters) merges its chunks in the same launch (O = sum_c exp(L_c - L)
+ *     O_c, L = ln sum_c exp(L_c)); with B*H above the 2048 counters a second
+ *     launch merges instead.  One chunk: written directly.  P stays in fp32
+ *     here: nothing is rounded before P.V.
  *   - otherwise the attention kernel of fa_fwd: when there are no more work
  *     items than SMs, the keys of each item are split over several CTAs (at
  *     least 16 key tiles each) and the parts merged in the same launch.
@@ -163,7 +165,7 @@ int fa_fwd_noalloc(const void* q, const void* k, const void* v, void* o, float* 
  * *num_ctas = the attention kernel's grid, *num_split_items = items computed
  * in parts (merged inside the same launch).  For the decode kernels' shapes:
  * *num_ctas = chunks x B x H, *num_split_items = B x H when the keys are cut
- * into more than one chunk (merged by the second launch), else 0.  The paper has no counterpart;
+ * into more than one chunk, else 0.  The paper has no counterpart;
  * it exists so that callers can see how the work is divided.  Returns FA_OK, FA_ERR_NULL (an output pointer is NULL),
  * FA_ERR_INVALID_ARG (sizes as for fa_fwd), FA_ERR_DEVICE or FA_ERR_LAUNCH.
  */
