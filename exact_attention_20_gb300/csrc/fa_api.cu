@@ -94,12 +94,27 @@ DeviceInfo* device_info(int* dev_out) {
 
 // Host copy of the kernel's work accounting (decode_item, tiles_for, item_steps).
 struct PlanShape {
-  int Nq, BH, nkt, nrb;  // query rows, B*H, key tiles, row blocks
+  int Nq, BH, nkt, nrb;  // query rows, heads of the items, key tiles, row blocks
   bool causal;
+  bool paired;           // each item pairs two heads' single query tiles
 };
 
+// Items pair two heads when every head has one query tile (Nq <= 128), the
+// heads pair up evenly, and the pairs alone fill every CTA (with fewer, the
+// keys of each item would be split, and merging parts of 256 rows costs more
+// than the pairing gains); then B*H / 2 items of one row block.
+bool pairs_heads(int BH, int Nq, int num_ctas) {
+  return Nq <= fa::kBlockM && BH % 2 == 0 && BH / 2 >= num_ctas;
+}
+PlanShape plan_shape(int BH, int Nq, int Nk, bool causal, int num_ctas) {
+  const bool paired = pairs_heads(BH, Nq, num_ctas);
+  const int nkt = (Nk + fa::kBlockN - 1) / fa::kBlockN;
+  const int nrb = paired ? 1 : (Nq + fa::kItemRows - 1) / fa::kItemRows;
+  return PlanShape{Nq, paired ? BH / 2 : BH, nkt, nrb, causal, paired};
+}
+
 int host_tiles_for(const PlanShape& s, int rb, int t) {
-  const int r0 = rb * fa::kItemRows + t * fa::kBlockM;
+  const int r0 = fa::tile_row0(rb, t, s.paired);
   if (r0 >= s.Nq) return 0;
   return s.causal ? std::min(r0 / fa::kBlockN + 1, s.nkt) : s.nkt;
 }
@@ -282,10 +297,12 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.status = di->status;
   p.Nq = Nq;
   p.Nk = Nk;
-  p.BH = BH;
-  p.n_key_tiles = (Nk + fa::kBlockN - 1) / fa::kBlockN;
-  p.n_row_blocks = (Nq + fa::kItemRows - 1) / fa::kItemRows;
-  p.num_items = BH * p.n_row_blocks;
+  const PlanShape shape = plan_shape(BH, Nq, Nk, CAUSAL, num_ctas_for(di, max_ctas));
+  p.BH = shape.BH;
+  p.paired = shape.paired ? 1 : 0;
+  p.n_key_tiles = shape.nkt;
+  p.n_row_blocks = shape.nrb;
+  p.num_items = shape.BH * shape.nrb;
   p.qk_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.wait_limit_ns = wait_limit_ns;
   p.starve_kv = starve_kv;
@@ -294,7 +311,6 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.v_scale = sc.v;
   p.part_o = nullptr;
   p.part_lse = nullptr;
-  const PlanShape shape{Nq, BH, p.n_key_tiles, p.n_row_blocks, CAUSAL};
   int num_split = 0;
   const int grid = plan_launch(shape, num_ctas_for(di, max_ctas), max_ctas == 0, p, num_split);
   p.counters = nullptr;
@@ -579,13 +595,11 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
     *num_split_items = plan.n_chunks > 1 ? BH : 0;
     return FA_OK;
   }
-  const int nkt = (Nk + fa::kBlockN - 1) / fa::kBlockN;
-  const int nrb = (Nq + fa::kItemRows - 1) / fa::kItemRows;
   static fa::FwdParams p;
   int num_split = 0;
   std::lock_guard<std::mutex> plan_lock(g_plan_mu);
-  *num_ctas = plan_launch(PlanShape{Nq, BH, nkt, nrb, causal == 1}, num_ctas_for(di, 0), true, p,
-                          num_split);
+  const int ctas = num_ctas_for(di, 0);
+  *num_ctas = plan_launch(plan_shape(BH, Nq, Nk, causal == 1, ctas), ctas, true, p, num_split);
   *num_split_items = num_split;
   return FA_OK;
 }

@@ -1,5 +1,6 @@
 // Fused exact attention forward for sm_103a: one persistent CTA per SM, each
-// work item = two adjacent 128-row query tiles of one (batch, head).
+// work item = two adjacent 128-row query tiles of one (batch, head), or, when
+// every head has one tile, the tiles of two heads.
 //
 // The method is the FlashAttention-2 forward ("FlashAttention and kernels.",
 // sections "From a sum to an output row" and "FlashAttention's forward pass";
@@ -113,7 +114,8 @@ struct FwdParams {
   float* part_lse;         // workspace: [slot][256] fp32, the part's natural-log logsumexp
   int Nq;                  // query rows (of O and LSE)
   int Nk;                  // keys (of K and V)
-  int BH;
+  int BH;                  // heads the items run over: B*H, or B*H / 2 when paired
+  int paired;              // 1: item (0, bh) is query tile 0 of the two heads 2bh and 2bh+1 (Nq <= 128)
   int n_key_tiles;         // ceil(N / 128)
   int n_row_blocks;        // ceil(N / 256)
   int num_items;           // BH * n_row_blocks
@@ -159,12 +161,22 @@ __device__ __forceinline__ void decode_item(int item, const FwdParams& p, int& r
   decode_item_shape(item, p.BH, p.n_row_blocks, rb, bh);
 }
 
+// The head and first query row of query tile t of item (rb, bh).  An item
+// is normally two adjacent 128-row tiles of one head; with at most 128 query
+// rows (one tile per head) it pairs two heads instead, so that both query
+// tiles, and both softmax warpgroups, have work: each tile then streams its
+// own head's K and V.
+__host__ __device__ __forceinline__ int tile_head(int bh, int t, int paired) { return paired ? 2 * bh + t : bh; }
+__host__ __device__ __forceinline__ int tile_row0(int rb, int t, int paired) {
+  return paired ? 0 : rb * kItemRows + t * kBlockM;
+}
+
 // Number of key tiles query tile t of row block rb visits (0 if the tile
 // lies beyond the last query row).  Causal is the top-left mask: key j for
 // query i iff j <= i, so rows past the last key see every key tile.
 template <bool CAUSAL>
 __device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
-  const int r0 = rb * kItemRows + t * kBlockM;
+  const int r0 = tile_row0(rb, t, p.paired);
   if (r0 >= p.Nq) return 0;
   if (CAUSAL) return min(r0 / kBlockN + 1, p.n_key_tiles);
   return p.n_key_tiles;
@@ -273,15 +285,19 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
       ++q_loads[t];
       mbar_arrive_expect_tx(sy.q_full[t], C::kTileBytes);
       const uint32_t dst = sbase + C::kQOff + t * C::kTileBytes;
-      const int row = rb * kItemRows + t * kBlockM;
+      const int row = tile_row0(rb, t, p.paired);
+      const int head = tile_head(bh, t, p.paired);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s)
-        tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * (128 / E), row, bh, pol_q);
+        tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * (128 / E), row, head, pol_q);
     }
     if (p.starve_kv) continue;  // self-test: never deliver K/V
+    // per step: K then V (normal), or K of both heads then V of both (paired)
+    const int heads = p.paired ? 2 : 1;
     for (int j = ch.kb; j < ch.ke && ok; ++j) {
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      for (int n = 0; n < 2 * heads && ok; ++n) {
+        const int which = n / heads;
+        const int head = p.paired ? 2 * bh + n % heads : bh;
         const uint32_t slot = kv_count % C::kStages;
         const uint32_t par = ((kv_count / C::kStages) & 1u) ^ 1u;
         ok = wait_phase(sy.kv_empty0 + 8 * slot, par, sy, p, kSiteProducer);
@@ -293,11 +309,11 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
         if (E == 1 && which == 1) {
           // the FP8 path's V is stored transposed, [BH][D][keys]: the tile is
           // D rows of 128 keys
-          tma_load_3d_hint(dst, map, full, j * kBlockN, 0, bh, pol_kv);
+          tma_load_3d_hint(dst, map, full, j * kBlockN, 0, head, pol_kv);
         } else {
 #pragma unroll
           for (int s = 0; s < C::kSlabs; ++s)
-            tma_load_3d_hint(dst + s * kSlabBytes, map, full, s * (128 / E), j * kBlockN, bh, pol_kv);
+            tma_load_3d_hint(dst + s * kSlabBytes, map, full, s * (128 / E), j * kBlockN, head, pol_kv);
         }
         ++kv_count;
       }
@@ -388,9 +404,13 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
     ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
   };
   auto wait_full = [&](uint32_t c) { wait_voted(full(c), (c / C::kStages) & 1u); };
+  // A K/V slot is released twice: once per query tile normally, and both
+  // times by its one user when the item pairs two heads.
+  const int rel = p.paired ? 2 : 1;
   auto release_unused = [&](uint32_t c) {  // a K/V tile this query tile skips
     wait_full(c);                          // its previous phase is then complete
-    if (ok && leader) mbar_arrive(empty(c));
+    if (ok && leader)
+      for (int i = 0; i < rel; ++i) mbar_arrive(empty(c));
   };
   if (t == 1 && leader) mbar_arrive(sy.turn[0]);  // tile 0 takes the first turn
 
@@ -406,6 +426,9 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
     const int kb = ch.kb;
     const int ne = min(ch.ke, tiles_for<CAUSAL>(ch.rb, t, p));
     const int n_steps = ch.ke - kb;  // both issuers walk the same steps
+    const uint32_t kvps = p.paired ? 4u : 2u;   // K/V slots per step
+    const uint32_t koff = p.paired ? t : 0u;    // this tile's K among them
+    const uint32_t voff = p.paired ? 2u + t : 1u;  // and its V
     if (ne > kb) {
       wait_voted(bar_q_full, q_uses & 1u);
       ++q_uses;
@@ -414,8 +437,9 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
     for (int s = kb; s <= ch.ke && ok; ++s) {
       const bool do_pv = s - 1 >= kb && s - 1 < ne;
       const bool do_s = s < ne;
-      const uint32_t cv = kv_count + 2 * (s - 1 - kb) + 1;  // V_{s-1}
-      const uint32_t ck = kv_count + 2 * (s - kb);          // K_s
+      // slots per step: K, V (normal) or K of both heads, V of both (paired)
+      const uint32_t cv = kv_count + kvps * (s - 1 - kb) + voff;  // V_{s-1}
+      const uint32_t ck = kv_count + kvps * (s - kb) + koff;      // K_s
       // K/V (landed long before, as a rule) first, then the descriptors, and
       // the softmax's P last: once P is in, only the turn stands between it
       // and the products.
@@ -486,15 +510,17 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       if (do_s) umma_commit(bar_s_full);
       if (do_pv && !do_s) umma_commit(bar_o_done);
       if (do_s && s == ne - 1) umma_commit(bar_q_empty);
-      if (do_pv) umma_commit(empty(cv));
-      if (do_s) umma_commit(empty(ck));
+      for (int i = 0; i < rel; ++i) {
+        if (do_pv) umma_commit(empty(cv));
+        if (do_s) umma_commit(empty(ck));
+      }
       mbar_arrive(next_turn);
       }
       __syncwarp();
       if (!do_pv && s - 1 >= kb) release_unused(cv);
       if (!do_s && s < ch.ke) release_unused(ck);
     }
-    kv_count += 2 * n_steps;
+    kv_count += kvps * n_steps;
   }
   // Every MMA this thread issued must finish before tensor memory is released.
   if (leader) umma_commit(sy.drain);
@@ -598,10 +624,11 @@ template <int D>
 __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlots ps, int t, int quad,
                                         uint32_t tO, int* ctr, __nv_bfloat16* __restrict__ o,
                                         float* __restrict__ lse, const float* __restrict__ part_o,
-                                        const float* __restrict__ part_lse, int Nq) {
+                                        const float* __restrict__ part_lse, int Nq, int paired) {
   const int lane = threadIdx.x & 31;
-  const int r = t * kBlockM + quad * 32 + lane;  // row within the item
-  const int row = pm.rb * kItemRows + r;
+  const int r = t * kBlockM + quad * 32 + lane;  // row within the item (and its slot)
+  const int row = tile_row0(pm.rb, t, paired) + quad * 32 + lane;
+  const int head = tile_head(pm.bh, t, paired);
   // Every lane acquires the counter itself: the other parts' rows were
   // published (and fenced) before their arrivals were counted.  Then it is
   // reset for the next launch: every arrival for these rows has happened.
@@ -628,7 +655,7 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
   }
   const float inv_w = 1.f / wsum;
   const bool store = row < Nq;
-  __nv_bfloat16* orow = o + (static_cast<size_t>(pm.bh) * Nq + (store ? row : 0)) * D;
+  __nv_bfloat16* orow = o + (static_cast<size_t>(head) * Nq + (store ? row : 0)) * D;
   const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   const float* own_row = part_o + (static_cast<size_t>(pm.own_slot) * kItemRows + r) * D;
   const float f_own = pm.in_tmem ? w_own * pm.inv_l * inv_w : w_own * inv_w;
@@ -681,7 +708,7 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
       }
     }
   }
-  if (store) lse[static_cast<size_t>(pm.bh) * Nq + row] = m + logf(wsum);
+  if (store) lse[static_cast<size_t>(head) * Nq + row] = m + logf(wsum);
 }
 
 // ---------------------------------------------------------------------------
@@ -716,13 +743,13 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     int rb0, bh0;
     decode_item(item, p, rb0, bh0);
     const Chunk ch = chunk_of(item, item_steps<CAUSAL>(rb0, p), wr, sp, p);
-    const int rb = ch.rb, bh = ch.bh;
+    const int rb = ch.rb, bh = tile_head(ch.bh, t, p.paired);  // this query tile's head
     const int n = tiles_for<CAUSAL>(rb, t, p);       // key tiles of this query tile in the item
     const int ne = min(ch.ke, n);                    // ... and its part in this chunk: [kb, ne)
-    const int row = rb * kItemRows + t * kBlockM + row_in_tile;
+    const int row = tile_row0(rb, t, p.paired) + row_in_tile;
     // FP8 path: this query tile's scale (one per 128 query rows)
     const float sq = E == 1 ? p.q_scale[static_cast<size_t>(bh) * ((p.Nq + kBlockM - 1) / kBlockM) +
-                                        rb * kQTiles + t]
+                                        tile_row0(rb, t, p.paired) / kBlockM]
                             : 1.f;
     if (ne <= ch.kb) {
       // No key tile of this query tile lies in the chunk (past its diagonal).
@@ -975,7 +1002,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     for (int q = 0; q < kMaxPartsPerItem; ++q) ps.slot[q] = q < ps.n ? p.merge_slots[first + q] : -1;
     tc_fence_after_sync();
     merge_rows<D>(pm, ps, t, quad, tO, p.counters + pm.k * kCountersPerItem + t * 4 + quad, p.o, p.lse, p.part_o,
-                  p.part_lse, p.Nq);
+                  p.part_lse, p.Nq, p.paired);
   }
 }
 

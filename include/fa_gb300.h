@@ -71,7 +71,10 @@ enum fa_status {
  *   stream  : cudaStream_t as void*.
  *
  * Work division.  A work item is 256 query rows of one (b, h); its cost is
- * the key tiles of 128 its longer half visits.  With more items than SMs
+ * the key tiles of 128 its longer half visits.  When every (b, h) has at
+ * most 128 query rows, B*H is even and B*H / 2 is at least the number of
+ * SMs, an item instead pairs the query rows of two heads (each half of the
+ * item streaming its own head's K and V), so that both halves have work.  With more items than SMs
  * (or fewer, but with at least 16 key tiles per SM to share out),
  * the concatenated steps of all items are cut into one equal contiguous
  * range per CTA (at most one CTA per SM); an item cut between two CTAs is computed in parts, each

@@ -89,7 +89,7 @@ def _compare(o, lse, o_ref, lse_ref, v_deq, label):
     return stats
 
 
-@pytest.mark.parametrize("B,H,N", [(1, 2, 256), (2, 3, 300), (1, 4, 1000), (1, 1, 1), (1, 2, 129)])
+@pytest.mark.parametrize("B,H,N", [(1, 2, 256), (2, 3, 300), (1, 4, 1000), (1, 1, 1), (1, 2, 129), (1, 4, 100), (1, 320, 100)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_fp8_forward_every_element(fa, B, H, N, causal):
     q, k, v = make_qkv(B, H, N, 128, seed=61, device=DEV)

@@ -59,11 +59,28 @@ def test_rect_every_element(fa, B, H, Nq, Nk, d, causal):
 
 
 def test_decode_shape_splits_keys(fa):
+    # 8 heads of 128 rows: 8 items (too few to pair heads), each split
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     grid, nsplit = fa.plan(1, 8, 128, 128, False, n_keys=16384)
     assert nsplit == 8 and 8 < grid <= min(sms, 8 * 7)
     # too little work to share: whole items
     assert fa.plan(1, 2, 64, 128, False, n_keys=512) == (2, 0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rect_paired_heads(fa, d, causal):
+    # enough heads of <= 128 rows that each item pairs two heads' query tiles
+    # (two K/V streams per item) with every CTA busy: every element, every head
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 2 * sms + 16
+    q, k, v = _inputs(1, H, 100, 1000, d, seed=42)
+    scale = d ** -0.5
+    grid, _ = fa.plan(1, H, 100, d, causal, n_keys=1000)
+    assert grid == sms  # every CTA busy (stream-K may still cut items in two)
+    o, lse = fa.attention_rect(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert_close(compare(o, lse, *_oracle(q, k, v, scale, causal)), f"paired heads d={d} causal={causal}")
 
 
 @pytest.mark.parametrize("causal", [False, True])
