@@ -28,7 +28,7 @@ struct DeviceInfo {
   bool supported = false;
   int num_sms = 0;
   int* status = nullptr;
-  bool attr_set[2][2][2] = {};  // [FP8 path][d == 128][causal]
+  bool attr_set[2][2][2][2] = {};  // [FP8 path][d == 128][causal][items pair heads]
   bool decode_attr_set[2][3] = {};  // decode kernels: [d == 128][rows 1, 2, 4]
   // Workspace for the parts of split items, one per stream so that calls on
   // different streams never share it.  Allocated on a stream's first call.
@@ -278,13 +278,14 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
         !fa::encode_u8_3d(&tv, v, nk_pad, D, BH, fa::kBlockN, D))
       return FA_ERR_LAUNCH;
   }
+  const PlanShape shape = plan_shape(BH, Nq, Nk, CAUSAL, num_ctas_for(di, max_ctas));
+  // the kernel instance: items of one head's two query tiles, or paired heads
+  auto kernel = shape.paired ? fa::fa_fwd_kernel<D, CAUSAL, E, true> : fa::fa_fwd_kernel<D, CAUSAL, E, false>;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    bool& set = di->attr_set[E == 1][D == 128][CAUSAL];
+    bool& set = di->attr_set[E == 1][D == 128][CAUSAL][shape.paired];
     if (!set) {
-      if (cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, E>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::kSmemBytes) != cudaSuccess)
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
         return FA_ERR_LAUNCH;
       set = true;
     }
@@ -297,9 +298,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.status = di->status;
   p.Nq = Nq;
   p.Nk = Nk;
-  const PlanShape shape = plan_shape(BH, Nq, Nk, CAUSAL, num_ctas_for(di, max_ctas));
   p.BH = shape.BH;
-  p.paired = shape.paired ? 1 : 0;
   p.n_key_tiles = shape.nkt;
   p.n_row_blocks = shape.nrb;
   p.num_items = shape.BH * shape.nrb;
@@ -330,7 +329,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
     p.part_lse = ws + ws_slots(di) * fa::kItemRows * 128;
     p.counters = reinterpret_cast<int*>(ws + ws_counter_offset(di));
   }
-  fa::fa_fwd_kernel<D, CAUSAL, E><<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, fa::kNumThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_OK;
 }

@@ -114,8 +114,7 @@ struct FwdParams {
   float* part_lse;         // workspace: [slot][256] fp32, the part's natural-log logsumexp
   int Nq;                  // query rows (of O and LSE)
   int Nk;                  // keys (of K and V)
-  int BH;                  // heads the items run over: B*H, or B*H / 2 when paired
-  int paired;              // 1: item (0, bh) is query tile 0 of the two heads 2bh and 2bh+1 (Nq <= 128)
+  int BH;                  // heads the items run over: B*H, or B*H / 2 when the items pair heads
   int n_key_tiles;         // ceil(N / 128)
   int n_row_blocks;        // ceil(N / 256)
   int num_items;           // BH * n_row_blocks
@@ -174,18 +173,18 @@ __host__ __device__ __forceinline__ int tile_row0(int rb, int t, int paired) {
 // Number of key tiles query tile t of row block rb visits (0 if the tile
 // lies beyond the last query row).  Causal is the top-left mask: key j for
 // query i iff j <= i, so rows past the last key see every key tile.
-template <bool CAUSAL>
+template <bool CAUSAL, bool PAIRED>
 __device__ __forceinline__ int tiles_for(int rb, int t, const FwdParams& p) {
-  const int r0 = tile_row0(rb, t, p.paired);
+  const int r0 = tile_row0(rb, t, PAIRED);
   if (r0 >= p.Nq) return 0;
   if (CAUSAL) return min(r0 / kBlockN + 1, p.n_key_tiles);
   return p.n_key_tiles;
 }
 
 // Steps of an item: the key tiles its longer query tile visits.
-template <bool CAUSAL>
+template <bool CAUSAL, bool PAIRED>
 __device__ __forceinline__ int item_steps(int rb, const FwdParams& p) {
-  return max(tiles_for<CAUSAL>(rb, 0, p), tiles_for<CAUSAL>(rb, 1, p));
+  return max(tiles_for<CAUSAL, PAIRED>(rb, 0, p), tiles_for<CAUSAL, PAIRED>(rb, 1, p));
 }
 
 // One chunk of this CTA's range: key tiles [kb, ke) of one item.
@@ -248,7 +247,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL, int E = 2>
+template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              uint32_t sbase, const Sync& sy, const FwdParams& p) {
   using C = Cfg<D, E>;
@@ -263,7 +262,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
     const int item = chunk_item(q, wr);
     int rb, bh;
     decode_item(item, p, rb, bh);
-    const int nkv = item_steps<CAUSAL>(rb, p);
+    const int nkv = item_steps<CAUSAL, PAIRED>(rb, p);
     const Chunk ch = chunk_of(item, nkv, wr, sp, p);
     if (ch.slot >= 0 && ch.last) {
       // The CTA's last chunk is a part of a split item: its warps will most
@@ -279,25 +278,27 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
       }
     }
     for (int t = 0; t < kQTiles && ok; ++t) {
-      if (min(ch.ke, tiles_for<CAUSAL>(rb, t, p)) <= ch.kb) continue;  // no tile of its own here
+      if (min(ch.ke, tiles_for<CAUSAL, PAIRED>(rb, t, p)) <= ch.kb) continue;  // no tile of its own here
       ok = wait_phase(sy.q_empty[t], (q_loads[t] & 1u) ^ 1u, sy, p, kSiteProducer);
       if (!ok) break;
       ++q_loads[t];
       mbar_arrive_expect_tx(sy.q_full[t], C::kTileBytes);
       const uint32_t dst = sbase + C::kQOff + t * C::kTileBytes;
-      const int row = tile_row0(rb, t, p.paired);
-      const int head = tile_head(bh, t, p.paired);
+      const int row = tile_row0(rb, t, PAIRED);
+      const int head = tile_head(bh, t, PAIRED);
 #pragma unroll
       for (int s = 0; s < C::kSlabs; ++s)
         tma_load_3d_hint(dst + s * kSlabBytes, tmQ, sy.q_full[t], s * (128 / E), row, head, pol_q);
     }
     if (p.starve_kv) continue;  // self-test: never deliver K/V
     // per step: K then V (normal), or K of both heads then V of both (paired)
-    const int heads = p.paired ? 2 : 1;
+    const int heads = PAIRED ? 2 : 1;
     for (int j = ch.kb; j < ch.ke && ok; ++j) {
-      for (int n = 0; n < 2 * heads && ok; ++n) {
+#pragma unroll
+      for (int n = 0; n < 2 * heads; ++n) {
+        if (!ok) break;
         const int which = n / heads;
-        const int head = p.paired ? 2 * bh + n % heads : bh;
+        const int head = PAIRED ? 2 * bh + n % heads : bh;
         const uint32_t slot = kv_count % C::kStages;
         const uint32_t par = ((kv_count / C::kStages) & 1u) ^ 1u;
         ok = wait_phase(sy.kv_empty0 + 8 * slot, par, sy, p, kSiteProducer);
@@ -368,7 +369,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 // tile 0's group, tile 1's group, tile 0's next group, ...  Each tile's
 // instructions stay in one thread, in issue order, so P_t(j-1) is read before
 // S_t(j) overwrites the same tensor-memory columns.
-template <int D, bool CAUSAL, int E = 2>
+template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, const Sync& sy,
                                         const FwdParams& p) {
   using C = Cfg<D, E>;
@@ -406,7 +407,7 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
   auto wait_full = [&](uint32_t c) { wait_voted(full(c), (c / C::kStages) & 1u); };
   // A K/V slot is released twice: once per query tile normally, and both
   // times by its one user when the item pairs two heads.
-  const int rel = p.paired ? 2 : 1;
+  const int rel = PAIRED ? 2 : 1;
   auto release_unused = [&](uint32_t c) {  // a K/V tile this query tile skips
     wait_full(c);                          // its previous phase is then complete
     if (ok && leader)
@@ -420,15 +421,15 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
     const int item = chunk_item(q, wr);
     int rb0, bh0;
     decode_item(item, p, rb0, bh0);
-    const int nkv_item = item_steps<CAUSAL>(rb0, p);
+    const int nkv_item = item_steps<CAUSAL, PAIRED>(rb0, p);
     const Chunk ch = chunk_of(item, nkv_item, wr, sp, p);
     // this query tile's key tiles inside the chunk: [kb, ne)
     const int kb = ch.kb;
-    const int ne = min(ch.ke, tiles_for<CAUSAL>(ch.rb, t, p));
+    const int ne = min(ch.ke, tiles_for<CAUSAL, PAIRED>(ch.rb, t, p));
     const int n_steps = ch.ke - kb;  // both issuers walk the same steps
-    const uint32_t kvps = p.paired ? 4u : 2u;   // K/V slots per step
-    const uint32_t koff = p.paired ? t : 0u;    // this tile's K among them
-    const uint32_t voff = p.paired ? 2u + t : 1u;  // and its V
+    const uint32_t kvps = PAIRED ? 4u : 2u;   // K/V slots per step
+    const uint32_t koff = PAIRED ? t : 0u;    // this tile's K among them
+    const uint32_t voff = PAIRED ? 2u + t : 1u;  // and its V
     if (ne > kb) {
       wait_voted(bar_q_full, q_uses & 1u);
       ++q_uses;
@@ -714,7 +715,7 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
 // ---------------------------------------------------------------------------
 // Softmax / correction / epilogue warpgroup (128 threads, one row each)
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL, int E = 2>
+template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy, const FwdParams& p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -742,14 +743,14 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     const int item = chunk_item(q, wr);
     int rb0, bh0;
     decode_item(item, p, rb0, bh0);
-    const Chunk ch = chunk_of(item, item_steps<CAUSAL>(rb0, p), wr, sp, p);
-    const int rb = ch.rb, bh = tile_head(ch.bh, t, p.paired);  // this query tile's head
-    const int n = tiles_for<CAUSAL>(rb, t, p);       // key tiles of this query tile in the item
+    const Chunk ch = chunk_of(item, item_steps<CAUSAL, PAIRED>(rb0, p), wr, sp, p);
+    const int rb = ch.rb, bh = tile_head(ch.bh, t, PAIRED);  // this query tile's head
+    const int n = tiles_for<CAUSAL, PAIRED>(rb, t, p);       // key tiles of this query tile in the item
     const int ne = min(ch.ke, n);                    // ... and its part in this chunk: [kb, ne)
-    const int row = tile_row0(rb, t, p.paired) + row_in_tile;
+    const int row = tile_row0(rb, t, PAIRED) + row_in_tile;
     // FP8 path: this query tile's scale (one per 128 query rows)
     const float sq = E == 1 ? p.q_scale[static_cast<size_t>(bh) * ((p.Nq + kBlockM - 1) / kBlockM) +
-                                        tile_row0(rb, t, p.paired) / kBlockM]
+                                        tile_row0(rb, t, PAIRED) / kBlockM]
                             : 1.f;
     if (ne <= ch.kb) {
       // No key tile of this query tile lies in the chunk (past its diagonal).
@@ -1002,14 +1003,14 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     for (int q = 0; q < kMaxPartsPerItem; ++q) ps.slot[q] = q < ps.n ? p.merge_slots[first + q] : -1;
     tc_fence_after_sync();
     merge_rows<D>(pm, ps, t, quad, tO, p.counters + pm.k * kCountersPerItem + t * 4 + quad, p.o, p.lse, p.part_o,
-                  p.part_lse, p.Nq, p.paired);
+                  p.part_lse, p.Nq, PAIRED);
   }
 }
 
 // ---------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------
-template <int D, bool CAUSAL, int E = 2>
+template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -1083,15 +1084,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   if (warp >= 8) {
     setmaxnreg_dec<kRegsAux>();
     if (warp == kLoadWarp) {
-      if (lane == 0) run_producer<D, CAUSAL, E>(&tmQ, &tmK, &tmV, sbase, sy, p);
+      if (lane == 0) run_producer<D, CAUSAL, E, PAIRED>(&tmQ, &tmK, &tmV, sbase, sy, p);
       __syncwarp();
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      run_mma<D, CAUSAL, E>(warp - kMmaWarp, sbase, tmem, sy, p);
+      run_mma<D, CAUSAL, E, PAIRED>(warp - kMmaWarp, sbase, tmem, sy, p);
       __syncwarp();
     }
   } else {
     setmaxnreg_inc<kRegsSoftmax>();
-    run_softmax<D, CAUSAL, E>(warp >> 2, tmem, sy, p);
+    run_softmax<D, CAUSAL, E, PAIRED>(warp >> 2, tmem, sy, p);
   }
 
   tc_fence_before_sync();
