@@ -336,7 +336,7 @@ def plan(B: int, H: int, N: int, d: int, causal: bool = False,
     return grid.value, nsplit.value
 
 
-KERNELS_PER_CALL = 1  # every fa_fwd call is one kernel launch
+KERNELS_PER_CALL = 1  # an fa_fwd call at the bench sizes is one kernel launch (so is a decode call up to 2048 heads)
 BWD_KERNELS_PER_CALL = 3  # fa_bwd: prep (D, L, zero dQ accumulator), the backward kernel, dQ conversion
 
 
