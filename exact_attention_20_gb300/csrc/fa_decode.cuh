@@ -3,11 +3,11 @@
 //
 // The work is bound by reading K and V once (about half a FLOP per byte), so
 // no tensor core is used: a 128-row tile would be almost all padding rows.
-// Keys are cut into equal chunks, one CTA per (chunk, batch*head), sized so
-// that one wave fills every SM; each CTA streams its chunk with coalesced
-// loads (a warp reads one 2 * D-byte key row per load instruction) and keeps
-// an online softmax per warp (running maximum m, running sum l, rescaled
-// fp32 accumulator: "FlashAttention and kernels.", section "From a sum to an
+// Keys are cut into equal chunks, one CTA per (chunk, batch*head), about
+// eight CTAs per SM in all; each CTA streams its chunk through a
+// shared-memory ring filled by bulk copies, and each of its consumer warps
+// keeps an online softmax (running maximum m, running sum l, rescaled fp32
+// accumulator: "FlashAttention and kernels.", section "From a sum to an
 // output row").  The eight warps' states are combined through shared memory,
 // and the chunks' normalised partial outputs are merged through their
 // logsumexps ("FlashAttention and kernels.", the merge of partial states over
@@ -110,7 +110,6 @@ __device__ __forceinline__ float dot_share(const uint64_t* q2, const Packed<EPL>
   f2_unpack(s2, lo, hi);
   return lo + hi;
 }
-
 
 // One CTA: key chunk blockIdx.x of batch*head blockIdx.y, rows 0 .. Nq-1
 // (NQ >= Nq; rows past Nq are computed on zeros and never written).
