@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreadsAll, NQ == 4 ? 1 : 2) partial_kernel(c
     if (lane == 0) {
       const __nv_bfloat16* kg = p.k + (static_cast<size_t>(bh) * p.Nk + k_begin) * D;
       const __nv_bfloat16* vg = p.v + (static_cast<size_t>(bh) * p.Nk + k_begin) * D;
+      int issued = 0;
       for (int r = 0; r < n_rounds; ++r) {
         const int st = r % kStages;
         if (r >= kStages && !mbar_wait_bounded(empty(st), ((r / kStages) - 1) & 1, p.wait_limit_ns)) {
@@ -162,7 +163,12 @@ __global__ void __launch_bounds__(kThreadsAll, NQ == 4 ? 1 : 2) partial_kernel(c
         const size_t off = static_cast<size_t>(r) * kKeysPerRound * D;
         bulk_load(sbase + st * 2 * kBlockBytes, kg + off, bytes, full(st));
         bulk_load(sbase + st * 2 * kBlockBytes + kBlockBytes, vg + off, bytes, full(st));
+        issued = r + 1;
       }
+      // Drain: every copy issued has landed before the CTA can exit, also
+      // after a wait gave up (at most one round per stage can be in flight).
+      for (int r = max(0, issued - kStages); r < issued; ++r)
+        mbar_wait_bounded(full(r % kStages), (r / kStages) & 1, p.wait_limit_ns);
     }
     __syncwarp();
   }
