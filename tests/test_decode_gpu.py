@@ -6,8 +6,8 @@ on the same bf16 inputs, with the tolerances of the other GPU tests.  The
 shapes cover one to four rows (the three kernel instances), key counts that
 end inside a 64-key round, inside an eight-key group and on a chunk edge, a
 single key, keys that fit one chunk (no merge) and keys cut into many chunks
-(merged by a second launch), both head sizes, and the bench's decode shape
-in full.
+(merged in the same launch by the CTA that completes a head), both head
+sizes, and the bench's decode shape in full.
 """
 import numpy as np
 import pytest
