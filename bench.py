@@ -43,6 +43,18 @@ BWD_KERNEL_SOURCES = [
 ]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 FLUSH_BYTES = 256 << 20
+# tcgen05.mma (M = 128, kind::f16, bf16 in, fp32 accumulate) retires
+# 8,192 flop per clock per SM (measured on this GPU by a probe of the
+# instruction alone); times the SMs and the SM clock it is the per-clock peak
+TC_FLOP_PER_CLK_SM = 8192
+# NVIDIA's dense bf16 figure per GB300 GPU
+SPEC_BF16_TFLOPS = 2250.0
+
+
+def median(xs):
+    ys = sorted(xs)
+    n = len(ys)
+    return ys[n // 2] if n % 2 else 0.5 * (ys[n // 2 - 1] + ys[n // 2])
 
 
 def flops(w, causal):
@@ -183,13 +195,24 @@ def oracle_sample_rate(w, n_heads, seed=0):
 
     q, k, v = make_qkv(1, n_heads, w.N, w.d, seed=seed, values=w.values)
     qf, kf, vf = (t.float().numpy().astype(np.float64) for t in (q, k, v))
+    masks = [c for c in (False, True) if c in w.causal]
     t0 = time.perf_counter()
-    for causal in (False, True):
+    for causal in masks:
         oracle.attention(qf, kf, vf, w.scale, causal)
     dt = time.perf_counter() - t0
-    fl = sum(4.0 * n_heads * w.N * w.N * w.d / (2 if c else 1) for c in (False, True))
-    desc = f"{n_heads} of {w.B * w.H} heads of {w.name}, non-causal and causal, fp64 numpy"
+    fl = sum(4.0 * n_heads * w.N * w.N * w.d / (2 if c else 1) for c in masks)
+    names = " and ".join("causal" if c else "non-causal" for c in masks)
+    desc = f"{n_heads} of {w.B * w.H} heads of {w.name}, {names}, fp64 numpy"
     return fl / dt / 1e12, dt, desc
+
+
+def cpu_sample_heads(w, requested=None):
+    """Heads for the oracle's timed sample: as requested, else about 100
+    GFLOP of work (eight heads of the headline shape), at least one."""
+    if requested:
+        return requested
+    per_head = sum(4.0 * w.N * w.N * w.d / (2 if c else 1) for c in w.causal)
+    return max(1, min(w.B * w.H, int(round(1.03e11 / per_head))))
 
 
 def run_reference(args):
@@ -205,7 +228,7 @@ def run_reference(args):
         r, dt, desc = oracle_sample_rate(w, 1, seed=i)
         rates.append(r)
         times.append(dt)
-    fl = sum(4.0 * w.N * w.N * w.d / (2 if c else 1) for c in (False, True))
+    fl = sum(4.0 * w.N * w.N * w.d / (2 if c else 1) for c in w.causal)
     value = fl * len(times) / sum(times) / 1e12
     cores = os.cpu_count()
     line = {
@@ -214,7 +237,7 @@ def run_reference(args):
         "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "masks": ["non-causal", "causal"], "sample": "1 head per step"},
+                   "masks": ["causal" if c else "non-causal" for c in w.causal], "sample": "1 head per step"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": desc + " per step"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -283,7 +306,8 @@ def run_ours(args):
     barrier(world)
     per_mask_ms = [[evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(args.steps)]
                    for i in range(len(masks))]
-    step_ms = sum(sum(x) for x in per_mask_ms) / args.steps
+    # the median step (the masks run interleaved, one call each per step)
+    step_ms = median([sum(per_mask_ms[i][s] for i in range(len(masks))) for s in range(args.steps)])
     step_ms = max_over_ranks(step_ms, world)
     step_flops = sum(flops(w, c) for c in masks)
     value = world * step_flops / (step_ms * 1e-3) / 1e12
@@ -331,19 +355,28 @@ def run_ours(args):
 
     launches_per_step = fa.KERNELS_PER_CALL * len(masks)
     peak_burst, peak_sustained, peak_kind = measured_peaks()
-    dom = 0  # the non-causal launch carries two thirds of the step
-    dom_ms = sum(per_mask_ms[dom]) / args.steps
+    # the per-clock peak: every SM's tensor core at the SM clock sampled
+    # during the timed region (the pages define 100 % as operations per clock
+    # per SM times the clock the kernel ran at)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks["sm_mhz"] if clocks else None
+    clock_peak = sms * TC_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12 if mhz else None
+    dom = 0  # the first mask of the step: non-causal where the workload has it
+    dom_ms = median(per_mask_ms[dom])
     achieved = flops(w, masks[dom]) / (dom_ms * 1e-3) / 1e12
     per_mask = {}
     for i, c in enumerate(masks):
-        ms = sum(per_mask_ms[i]) / args.steps
+        ms = median(per_mask_ms[i])
         tf = flops(w, c) / (ms * 1e-3) / 1e12
         per_mask["causal" if c else "non-causal"] = {
-            "ms": ms, "tflops": tf, "frac_of_measured_peak": tf / peak_burst}
+            "ms": ms, "ms_mean": sum(per_mask_ms[i]) / len(per_mask_ms[i]), "tflops": tf,
+            "frac_of_measured_peak": tf / peak_burst,
+            "frac_of_clock_peak": tf / clock_peak if clock_peak else None,
+            "frac_of_spec_peak": tf / SPEC_BF16_TFLOPS}
 
     cpu = None
     if not args.no_cpu_baseline:
-        rate, dt, desc = oracle_sample_rate(w, args.cpu_heads)
+        rate, dt, desc = oracle_sample_rate(w, cpu_sample_heads(w, args.cpu_heads))
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{desc}; {dt:.1f} s; BLAS products on all cores, elementwise steps single-threaded"}
 
@@ -360,6 +393,13 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_burst,
                      "unit": "TFLOP/s", "frac": achieved / peak_burst,
                      "peak_kind": f"{peak_kind} bf16 dense, burst",
+                     "clock_peak": clock_peak, "frac_of_clock_peak": achieved / clock_peak if clock_peak else None,
+                     "clock_peak_kind": (f"{sms} SMs x {TC_FLOP_PER_CLK_SM} flop/clk/SM (tcgen05.mma M=128 kind::f16, "
+                                         f"measured by a probe on this GPU) x the median SM clock sampled in the "
+                                         f"timed region"),
+                     "spec_peak": SPEC_BF16_TFLOPS, "frac_of_spec_peak": achieved / SPEC_BF16_TFLOPS,
+                     "spec_peak_kind": "NVIDIA's dense bf16 figure per GB300 GPU (36 PFLOP/s per 8 GPUs with 2:4 sparsity)",
+                     "statistic": "median of the timed steps",
                      "kernel": f"fa_fwd_kernel<{w.d},{str(masks[dom]).lower()}>",
                      "timed_span": "one fa_fwd call = one launch of this kernel (split items merged inside it)",
                      "traffic": recorded_traffic(w.name, masks[dom])},
@@ -418,7 +458,7 @@ def run_decode(args):
             e1.record()
         torch.cuda.synchronize(dev)
         sampler.mark("t1")
-        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        ms = median([a.elapsed_time(b) for a, b in evs])
         nbytes = B * H * (2 * Nq * d * 2 + 2 * Nk * d * 2 + Nq * 4)
         grid, nsplit = fa.plan(B, H, Nq, d, False, n_keys=Nk)
         per_shape[f"B{B}-H{H}-Nq{Nq}-Nk{Nk}-d{d}"] = {
@@ -479,7 +519,7 @@ def run_backward(args):
             e1.record()
         torch.cuda.synchronize(dev)
         sampler.mark("t1")
-        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        ms = median([a.elapsed_time(b) for a, b in evs])
         f = 2.5 * flops(w, causal)
         per_mask["causal" if causal else "non-causal"] = {
             "ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "frac_of_measured_peak": f / (ms * 1e-3) / 1e12 / peak}
@@ -546,7 +586,7 @@ def run_fp8(args):
             e1.record()
         torch.cuda.synchronize(dev)
         sampler.mark("t1")
-        ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+        ms = median([a.elapsed_time(b) for a, b in evs])
         f = flops(w, causal)
         per_mask["causal" if causal else "non-causal"] = {
             "ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "frac_of_fp8_peak": f / (ms * 1e-3) / 1e12 / peak8}
@@ -589,7 +629,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-heads", type=int, default=8)
+    ap.add_argument("--cpu-heads", type=int, default=None,
+                    help="heads of the oracle's CPU sample (default: about 100 GFLOP of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode", action="store_true",
                     help="the few-query-rows shapes through fa_fwd_rect (HBM-bound), "

@@ -236,13 +236,17 @@ void remember_fixed_scratch(DeviceInfo* di, float* ws) {
   di->fixed_scratch.push_back(ws);
 }
 
+// This stream's workspace, allocated on its first splitting call.  Its
+// arrival counters are zeroed on `stream` itself, so the kernel that follows
+// on the same stream is ordered after the clear whatever kind of stream it
+// is (a non-blocking stream is not ordered after the legacy default stream).
 float* stream_workspace(DeviceInfo* di, cudaStream_t stream) {
   std::lock_guard<std::mutex> lock(g_mu);
   for (auto& w : di->workspaces)
     if (w.first == stream) return w.second;
   float* ptr = nullptr;
   if (cudaMalloc(&ptr, ws_bytes(di)) != cudaSuccess) return nullptr;
-  if (cudaMemset(ptr + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int)) != cudaSuccess) {
+  if (cudaMemsetAsync(ptr + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int), stream) != cudaSuccess) {
     cudaFree(ptr);
     return nullptr;
   }
@@ -543,24 +547,45 @@ int fa_get_device_status(void* stream) {
   if (di == nullptr) return FA_ERR_LAUNCH;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int h = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
-  if (cudaMemcpy(&h, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&h, di->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
     return FA_ERR_LAUNCH;
   if (h == 0) return FA_OK;
-  const int zero = 0;
-  if (cudaMemcpy(di->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
-    return FA_ERR_LAUNCH;
-  // A kernel that gave up may have left arrival counters of split items
-  // non-zero: clear them in every workspace and scratch of this device.
+  // A kernel that gave up may have left the arrival counters of some
+  // workspace or scratch non-zero, and the status word does not say which
+  // stream's kernel it was.  Once every stream of the device is idle, clear
+  // the status word and every area's counters, ordered on `stream`, and wait
+  // for the clears before returning.
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_LAUNCH;
   {
     std::lock_guard<std::mutex> lock(g_mu);
+    if (cudaMemsetAsync(di->status, 0, sizeof(int), s) != cudaSuccess) return FA_ERR_LAUNCH;
     std::vector<float*> areas = di->fixed_scratch;
     for (auto& w : di->workspaces) areas.push_back(w.second);
     for (float* a : areas)
-      if (cudaMemset(a + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int)) != cudaSuccess)
+      if (cudaMemsetAsync(a + ws_counter_offset(di), 0, fa::kNumCounters * sizeof(int), s) != cudaSuccess)
         return FA_ERR_LAUNCH;
   }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
   return FA_ERR_DEVICE_TIMEOUT;
+}
+
+int fa_release_stream(void* stream) {
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (di == nullptr) return FA_ERR_LAUNCH;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_LAUNCH;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (size_t i = 0; i < di->workspaces.size(); ++i) {
+      if (di->workspaces[i].first != s) continue;
+      if (cudaFree(di->workspaces[i].second) != cudaSuccess) return FA_ERR_LAUNCH;
+      di->workspaces.erase(di->workspaces.begin() + static_cast<long>(i));
+      break;
+    }
+  }
+  return fa_internal::release_bwd_workspace(dev, s) ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_watchdog_selftest(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -175,6 +175,21 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
 
 }  // namespace
 
+namespace fa_internal {
+
+bool release_bwd_workspace(int dev, void* stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (size_t i = 0; i < g_ws.size(); ++i) {
+    if (g_ws[i].dev != dev || g_ws[i].stream != static_cast<cudaStream_t>(stream)) continue;
+    const bool ok = cudaFree(g_ws[i].ptr) == cudaSuccess;
+    g_ws.erase(g_ws.begin() + static_cast<long>(i));
+    return ok;
+  }
+  return true;
+}
+
+}  // namespace fa_internal
+
 extern "C" {
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,

@@ -32,6 +32,10 @@ struct DeviceView {
 };
 bool current_device(DeviceView* out);
 
+// Frees the backward's workspace of `stream` on device `dev`, if it has one
+// (the caller has synchronised the stream).  False when cudaFree failed.
+bool release_bwd_workspace(int dev, void* stream);
+
 // Wait limit of every pipeline wait inside the kernels, in nanoseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

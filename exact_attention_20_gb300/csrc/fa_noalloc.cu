@@ -54,6 +54,11 @@ extern "C" int fa_fwd_noalloc(const void* q, const void* k, const void* v, void*
                               int B, int H, int N, int d, int causal, float scale, void* stream) {
   const int rc = fa_internal::check_fwd_args(q, k, v, o, lse, B, H, N, d, causal, scale);
   if (rc != FA_OK) return rc;
+  // the device first, as fa_fwd does: the module that holds the scratch is
+  // built for sm_103a only and does not load on another device
+  fa_internal::DeviceView view;
+  if (!fa_internal::current_device(&view)) return FA_ERR_LAUNCH;
+  if (!view.supported) return FA_ERR_DEVICE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
   float* ptr = scratch_address(dev);

@@ -39,6 +39,7 @@ SIGNATURES = {
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_get_device_status": (_I, [_P]),
+    "fa_release_stream": (_I, [_P]),
     "fa_watchdog_selftest": (_I, [_P, _P, _P, _P, _P, _I, _P]),
     "fa_version": (_I, []),
 }
@@ -343,6 +344,13 @@ BWD_KERNELS_PER_CALL = 3  # fa_bwd: prep (D, L, zero dQ accumulator), the backwa
 def device_status(stream=None) -> int:
     """FA_OK, or FA_ERR_DEVICE_TIMEOUT if a kernel gave up on a wait (clears the record)."""
     return lib().fa_get_device_status(_stream_handle(stream))
+
+
+def release_stream(stream=None) -> None:
+    """Frees the library's workspaces for `stream` (after synchronising it)."""
+    rc = lib().fa_release_stream(_stream_handle(stream))
+    if rc != FA_OK:
+        raise FAError(rc)
 
 
 def watchdog_selftest(limit_ms: int = 100, device="cuda") -> int:

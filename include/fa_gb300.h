@@ -25,11 +25,17 @@
  *     40 MB on a GB300) plus 2048 counters for the parts of split work
  *     items, allocated (and its counters zeroed) on the
  *     first fa_fwd on that stream that splits an item (or splits the keys
- *     of a decode call, whose chunk partials use its first part) and kept
- *     until the process exits; and, per stream, the backward's workspace (see
+ *     of a decode call, whose chunk partials use its first part), with the
+ *     counters cleared on that stream, and kept until fa_release_stream or
+ *     the end of the process; and, per stream, the backward's workspace (see
  *     fa_bwd).  fa_fwd_noalloc and fa_quantize_fp8 allocate nothing.  Calls
  *     on one stream reuse its workspaces in stream order; calls on different
- *     streams never share one.
+ *     streams never share one.  A caller that creates many short-lived
+ *     streams releases each one's workspaces with fa_release_stream.
+ *   - The library keeps per-device state for the life of the process (the
+ *     device's properties, the status word's and fa_fwd_noalloc's scratch
+ *     addresses, the workspaces).  It does not survive cudaDeviceReset: do
+ *     not call the library on a device after resetting it.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream) and return a status code.
  *   - Status 0 is FA_OK.  A negative status is returned for an error found
@@ -126,9 +132,12 @@ int fa_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse
 
 /*
  * fa_fwd_noalloc — fa_fwd (same arguments, kernels, work division and
- * results) with no device allocation at any call: the parts of split items
- * go to one static scratch array of FA_NOALLOC_SCRATCH_BYTES per device
- * instead of the per-stream workspace.  The paper has no counterpart; it is
+ * results, bit for bit) with no device allocation at any call: the parts of
+ * split items go to one static scratch array of FA_NOALLOC_SCRATCH_BYTES per
+ * device instead of the per-stream workspace.  One exception: the decode
+ * shapes (causal = 0 and N <= 4), which fa_fwd sends to the decode kernels,
+ * run the attention kernel here (its results then agree with fa_fwd's within
+ * the bf16 path's tolerance, not bit for bit).  The paper has no counterpart; it is
  * for callers that must not allocate during a call, such as a server that
  * reserves its whole memory budget at start-up, or one that cannot afford a
  * cudaMalloc/cudaFree blocking on work queued on other streams.
@@ -263,10 +272,25 @@ const char* fa_strerror(int code);
  * on the current device gave up on a pipeline wait (every wait inside the
  * kernel is bounded in time; on expiry the kernel records the failure, stops
  * its pipeline, releases tensor memory and exits instead of hanging).
- * Synchronises `stream`, returns FA_OK or FA_ERR_DEVICE_TIMEOUT, and clears
- * the recorded state.  Returns FA_ERR_LAUNCH if the status cannot be read.
+ * Reads the device's status word on `stream` (after the work queued there)
+ * and returns FA_OK or FA_ERR_DEVICE_TIMEOUT.  On a timeout it then waits for
+ * the whole device (cudaDeviceSynchronize), and clears the status word and
+ * the split-item counters of every workspace and of fa_fwd_noalloc's scratch
+ * on `stream`, waiting for the clears; call it then with no other call of
+ * this library in flight on the device (it is the recovery path).  Returns
+ * FA_ERR_LAUNCH if a CUDA call fails.
  */
 int fa_get_device_status(void* stream);
+
+/*
+ * fa_release_stream — frees the workspaces (forward and backward) that this
+ * library keeps for `stream` on the current device, after synchronising the
+ * stream.  A later call on the stream allocates them again.  Call it before
+ * destroying a stream the library has used, when streams are short-lived.
+ * The paper has no counterpart.  Returns FA_OK, or FA_ERR_LAUNCH if a CUDA
+ * call fails.
+ */
+int fa_release_stream(void* stream);
 
 /*
  * fa_watchdog_selftest — launches one small forward whose load warp is told

@@ -3,16 +3,22 @@
 Tolerances (fixed for this method): max|dO| <= 1e-2 and mean|dO| <= 1e-3 on
 bf16 O, |dLSE| <= 1e-3 in fp32.
 
-"On bf16 O" is read as the error of the bf16 output beyond the rounding that
-bf16 itself forces: for each element, dO = |O_gpu - O_ref| - |RN(O_ref) - O_ref|
-(never negative, zero when the GPU returns the correctly rounded value), and
-both the maximum and the mean are taken over that,
-where RN rounds the fp64 oracle value to the nearest bf16.  Where |O| >= 4 the
-bf16 grid spacing is 2^-5, so the nearest bf16 value can lie up to 0.0156 from
-the exact answer and no bf16 output could meet 1e-2 there.  The plain
-difference (``max_do_raw``, and ``max_do_raw_below4`` over |O| < 4) and the
-difference against the rounded oracle (``max_do_bf16``) are reported for
-diagnosis, not asserted.
+Asserted on every comparison:
+
+- the plain mean, mean|O_gpu - O_ref| over all elements, <= 1e-3;
+- the plain maximum, max|O_gpu - O_ref| over the elements with |O_ref| < 2,
+  <= 1e-2.  There the bf16 spacing is at most 2^-7 (a correctly rounded
+  output is within 0.0039 of the exact value), so the bound leaves the
+  kernel's own error at least 0.006;
+- for the elements with |O_ref| >= 2, the error beyond the rounding bf16
+  itself forces, |O_gpu - O_ref| - |RN(O_ref) - O_ref| <= 1e-2, where RN
+  rounds the fp64 oracle value to the nearest bf16.  From 2 on the bf16
+  spacing is 2^-6 or more: at [4, 8) the nearest bf16 value alone can lie
+  0.0156 from the exact answer, so no bf16 output could meet the plain
+  bound there, and at [2, 4) the half spacing (0.0078) leaves too little of
+  the bound to the kernel.  The plain maximum over [2, 4) is reported
+  (``max_do_raw_2to4``) next to the asserted figures;
+- max|LSE_gpu - LSE_ref| <= 1e-3 and no NaN.
 """
 from __future__ import annotations
 
@@ -24,6 +30,8 @@ import oracle
 MAX_DO = 1e-2
 MEAN_DO = 1e-3
 MAX_DLSE = 1e-3
+# below this |O| the plain difference is held to MAX_DO (bf16 spacing <= 2^-7)
+BF16_FINE = 2.0
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -40,20 +48,24 @@ def compare(o_gpu, lse_gpu, o_ref64, lse_ref64):
     lg = to_f64(lse_gpu)
     rn = round_bf16(o_ref64)
     d_raw = np.abs(og - o_ref64)
-    d_o = d_raw - np.abs(rn - o_ref64)          # beyond the unavoidable bf16 rounding
+    excess = d_raw - np.abs(rn - o_ref64)       # beyond the unavoidable bf16 rounding
     d_bf16 = np.abs(og - rn)
     d_l = np.abs(lg - lse_ref64)
-    below4 = np.abs(o_ref64) < 4.0
+    mag = np.abs(o_ref64)
+    below2 = mag < BF16_FINE
+    mid = (mag >= BF16_FINE) & (mag < 4.0)
     worst = np.unravel_index(np.argmax(d_raw), d_raw.shape)
     return {
-        "max_do": float(d_o.max()),
-        "mean_do": float(d_o.mean()),
+        "max_do_raw_below2": float(d_raw[below2].max()) if below2.any() else 0.0,
+        "max_excess_from2": float(excess[~below2].max()) if (~below2).any() else 0.0,
         "mean_do_raw": float(d_raw.mean()),
         "max_dlse": float(d_l.max()),
         "max_do_raw": float(d_raw.max()),
-        "max_do_raw_below4": float(d_raw[below4].max()) if below4.any() else 0.0,
+        "max_do_raw_2to4": float(d_raw[mid].max()) if mid.any() else 0.0,
+        "n_from2": int((~below2).sum()),
         "n_raw_over_1e-2": int((d_raw > MAX_DO).sum()),
         "max_do_bf16": float(d_bf16.max()),
+        "mean_excess": float(excess.mean()),
         "o_at_worst_raw": float(o_ref64[worst]),
         "nan": bool(np.isnan(og).any() or np.isnan(lg).any()),
     }
@@ -61,8 +73,9 @@ def compare(o_gpu, lse_gpu, o_ref64, lse_ref64):
 
 def assert_close(stats, label=""):
     assert not stats["nan"], f"{label}: NaN in output {stats}"
-    assert stats["max_do"] <= MAX_DO, f"{label}: max|dO| {stats}"
-    assert stats["mean_do"] <= MEAN_DO, f"{label}: mean|dO| {stats}"
+    assert stats["mean_do_raw"] <= MEAN_DO, f"{label}: mean|dO| {stats}"
+    assert stats["max_do_raw_below2"] <= MAX_DO, f"{label}: max|dO| where |O|<2 {stats}"
+    assert stats["max_excess_from2"] <= MAX_DO, f"{label}: max|dO| beyond bf16 rounding where |O|>=2 {stats}"
     assert stats["max_dlse"] <= MAX_DLSE, f"{label}: max|dLSE| {stats}"
 
 

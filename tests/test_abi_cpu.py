@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     assert names == ["fa_bwd", "fa_fwd", "fa_fwd_fp8", "fa_fwd_noalloc", "fa_fwd_plan", "fa_fwd_rect",
-                     "fa_get_device_status", "fa_quantize_fp8", "fa_strerror", "fa_version",
+                     "fa_get_device_status", "fa_quantize_fp8", "fa_release_stream", "fa_strerror", "fa_version",
                      "fa_watchdog_selftest"]
 
 

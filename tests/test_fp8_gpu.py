@@ -14,7 +14,7 @@ import torch
 
 from exact_attention_20_gb300 import build as fa_build
 from exact_attention_20_gb300.inputs import make_qkv
-from tests.parity import round_bf16, to_f64
+from tests.parity import BF16_FINE, round_bf16, to_f64
 
 import oracle
 from oracle import fp8 as ofp8
@@ -24,9 +24,15 @@ DEV = "cuda"
 
 # O tolerance: P in e4m3 moves each weight of the average by up to 2^-4
 # relative (round to nearest), so the output by at most 2^-4 of the spread of
-# the value rows it averages; these bounds are in units of max |V|.
-FP8_MAX_DO = 2.0 ** -4
-FP8_MEAN_DO = 2.0 ** -8
+# the value rows it averages, and the weights' errors are independent, so
+# over many keys they mostly cancel.  The bounds are in units of max |V|:
+# 2^-5 for the maximum and 2^-9 for the mean, about twice the largest
+# errors measured on these workloads (1.5 % and 0.07 % of max |V|).
+# As for the bf16 path, the plain difference is bounded where |O| < 2 and
+# the error beyond the output's own bf16 rounding where |O| >= 2; the mean
+# is the plain one.
+FP8_MAX_DO = 2.0 ** -5
+FP8_MEAN_DO = 2.0 ** -9
 FP8_MAX_DLSE = 1e-3
 
 
@@ -77,9 +83,11 @@ def _oracle_fp8(q, k, v, scale, causal):
 def _compare(o, lse, o_ref, lse_ref, v_deq, label):
     og, lg = to_f64(o), to_f64(lse)
     vmax = np.abs(v_deq).max()
-    d_o = np.maximum(np.abs(og - o_ref) - np.abs(round_bf16(o_ref) - o_ref), 0.0) / vmax
+    d_raw = np.abs(og - o_ref)
+    excess = d_raw - np.abs(round_bf16(o_ref) - o_ref)
+    d_o = np.where(np.abs(o_ref) < BF16_FINE, d_raw, excess) / vmax
     d_l = np.abs(lg - lse_ref)
-    stats = {"max_do_rel_vmax": float(d_o.max()), "mean_do_rel_vmax": float(d_o.mean()),
+    stats = {"max_do_rel_vmax": float(d_o.max()), "mean_do_rel_vmax": float(d_raw.mean() / vmax),
              "max_dlse": float(d_l.max()), "nan": bool(np.isnan(og).any())}
     print(f"\nfp8 {label}: {stats}")
     assert not stats["nan"], label
