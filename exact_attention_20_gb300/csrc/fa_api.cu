@@ -125,12 +125,30 @@ int host_item_steps(const PlanShape& s, int item) {
   return std::max(host_tiles_for(s, rb, 0), host_tiles_for(s, rb, 1));
 }
 
+// What a split item costs its CTAs beyond its steps, in steps: publishing
+// the parts (fp32 O of 256 rows) and merging them.  Measured on short items
+// (1024 tokens, d = 64: whole items faster by 10-20 %) against long ones
+// (3001 and 4096 tokens: split faster by 5-25 %).
+constexpr long long kMergeSteps = 4;
+
+// The longest CTA's steps when each CTA takes a contiguous run of whole
+// items (ceil(items / grid) of them), as plan_launch's fallback assigns them.
+long long whole_item_makespan(const std::vector<long long>& start, int items, int grid) {
+  const int per = (items + grid - 1) / grid;
+  long long worst = 0;
+  for (int a = 0; a < items; a += per) worst = std::max(worst, start[std::min(items, a + per)] - start[a]);
+  return worst;
+}
+
 // Splits the concatenated steps of all items into `grid` equal contiguous
 // ranges (one per CTA) and lists the items that end up in several parts.
-// With no more items than SMs the keys are split only when every CTA keeps
-// at least 16 steps; otherwise each CTA takes one whole item.
-// Returns false when a split would need more parts per item than the merge
-// takes; the caller then uses whole items.  num_split = split items.
+// With more items than SMs, the ranges are used only when their length plus
+// a merge's cost is below the longest run of whole items.  With no more
+// items than SMs the keys are split only when every CTA keeps at least 16
+// steps; otherwise each CTA takes one whole item.
+// Returns false when whole items are the better plan or a split would need
+// more parts per item than the merge takes; the caller then uses whole
+// items.  num_split = split items.
 bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams& p, int& grid,
                int& num_split) {
   const int items = s.BH * s.nrb;
@@ -141,6 +159,9 @@ bool make_plan(const PlanShape& s, int num_ctas, bool allow_split, fa::FwdParams
   for (int i = 0; i < items; ++i) start[i + 1] = start[i] + host_item_steps(s, i);
   const long long W = start[items];
   grid = num_ctas;
+  if (items > num_ctas &&
+      whole_item_makespan(start, items, num_ctas) <= (W + num_ctas - 1) / num_ctas + kMergeSteps)
+    return false;
   if (items <= num_ctas) {
     // Few items (few query rows over many keys, the decode shape): their
     // keys are split over more CTAs while each CTA keeps enough steps to

@@ -144,9 +144,11 @@ def test_identical_keys_give_mean_of_visible_values(fa):
                                      (4, 40, 1000, 64), (1, 33, 2304, 128), (1, 10, 4096, 64)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_guard_bands_untouched(fa, B, H, N, d, causal):
-    # the last three shapes have more work items than SMs, so items are split
-    # across CTAs and merged; with 152 SMs, (1, 10, 4096) causal has ranges of
-    # about 18 steps against items of up to 32, so some items have three parts
+    # the last three shapes have more work items than SMs: (4, 40, 1000) and
+    # (1, 10, 4096) have items split across CTAs and merged (with 152 SMs,
+    # (1, 10, 4096) causal has ranges of about 18 steps against items of up to
+    # 32, so some items have three parts); (1, 33, 2304) has short items, which
+    # the plan keeps whole, two or three to a CTA
     G = 4096
     q, k, v = make_qkv(B, H, N, d, seed=9, device=DEV)
     n_o, n_l = B * H * N * d, B * H * N
