@@ -51,8 +51,15 @@ constexpr uint32_t kRegsSoftmax = 192;
 static_assert(128 * kRegsAux + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds the launch");
 constexpr uint32_t kTmemCols = 512;
 // The reference maximum moves only when a tile's maximum exceeds it by more
-// than this many log2 units (so exponentials stay <= 2^8 = 256).
-constexpr float kRescaleThreshold = 8.0f;
+// than this many log2 units, so exponentials stay <= 2^threshold.  With FP8
+// operands P is rounded to e4m3 (largest finite value 448): 8, P <= 256.
+// With bf16, P and the fp32 sums keep their relative precision at any
+// magnitude, and 32 keeps them far from overflow (P <= 2^32; the row sum of
+// at most 2^24 keys <= 2^56): a move, which costs the warp a second pass
+// over the tile and a rescale of O, then needs a jump of the row maximum by
+// a factor of 2^32 rather than 2^8.
+template <int E>
+constexpr float kRescaleThreshold = E == 1 ? 8.0f : 32.0f;
 
 // Codes recorded in the device status word when a wait gives up.
 constexpr int kSiteProducer = 1;
@@ -764,9 +771,10 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     // m_ref: the reference maximum the exponentials are taken against (log2
     // units, already times qk_scale).  It is moved only when a tile's maximum
     // exceeds it by more than kRescaleThreshold, so P = exp2(s*qk - m_ref) may
-    // reach 2^kRescaleThreshold.  l, lq and O all use the same m_ref, so the
-    // shift cancels in O = acc / lq and in L = m_ref + log2 l exactly as in the
-    // every-tile update ("Softmax, the safe way": a common shift factors out).
+    // reach 2^kRescaleThreshold (2^32 for bf16, 2^8 for e4m3).  l, lq and O
+    // all use the same m_ref, so the shift cancels in O = acc / lq and in
+    // L = m_ref + log2 l exactly as in the every-tile update ("Softmax, the
+    // safe way": a common shift factors out).
     float m_ref = -INFINITY;
     float l = 0.f;        // running sum of exp2(s*qk - m_ref), for the logsumexp
     float lq = 0.f;       // the same terms rounded to bf16 (what P.V multiplies), for O
@@ -877,7 +885,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
         // The maximum first, then one pass (under the causal mask, whose short
         // items have many first tiles, this measured faster).
         const float m_tile = row_max();
-        if (m_tile > m_ref + kRescaleThreshold) {  // always taken on the first tile (m_ref = -inf)
+        if (m_tile > m_ref + kRescaleThreshold<E>) {  // always taken on the first tile (m_ref = -inf)
           alpha = ex2_approx(m_ref - m_tile);      // 0 when m_ref = -inf
           m_ref = m_tile;
         }
@@ -897,7 +905,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
 #pragma unroll 1
         for (int pass = 0; pass < 2; ++pass) {
           const float m_tile = exp_pass(m_ref == -INFINITY ? 0.f : m_ref, true);
-          const bool move = m_tile > m_ref + kRescaleThreshold;
+          const bool move = m_tile > m_ref + kRescaleThreshold<E>;
           if (!__any_sync(0xffffffffu, move)) break;
           if (move) {  // rare: move this row's reference, then the warp takes the pass again
             alpha = ex2_approx(m_ref - m_tile);

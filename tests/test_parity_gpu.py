@@ -91,25 +91,32 @@ def test_batch_head_indexing(fa, B, H, N, d, causal):
     assert_close(compare(o, lse, *oracle_full(q, k, v, 0.1, causal)), f"{B}x{H}x{N}x{d}")
 
 
+# Keys of 1.5 in the last tile raise each row's maximum there by about 20
+# (d = 128) or 10 (d = 64) log2 units: below the bf16 path's rescale threshold
+# of 32, so P grows past 1 against the old reference and nothing is rescaled.
+# Keys of 5.0 raise it by about 65 or 46: the reference moves, the tile is
+# exponentiated again and the accumulator rescaled.
+@pytest.mark.parametrize("k_last", [1.5, 5.0])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_max_in_last_key_tile(fa, d, causal):
+def test_max_in_last_key_tile(fa, d, causal, k_last):
     # the largest scores of every row sit in the last key tile, so a missing
     # rescale of the accumulator fails loudly (Break It #2 of the gtadkapally lesson)
     N = 1000
     q, k, v = make_qkv(1, 2, N, d, seed=77, device=DEV)
     q = q.float().abs().to(torch.bfloat16)
     k = k.clone()
-    k[:, :, N - 8:, :] = 1.5
+    k[:, :, N - 8:, :] = k_last
     o, lse = run(fa, q, k, v, causal, d ** -0.5)
     assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "max-last")
 
 
+@pytest.mark.parametrize("k_last", [1.5, 5.0])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_max_jumps_in_some_rows_only(fa, d, causal):
-    # even rows see a score jump of about 10-20 (log2 units) in the last key
-    # tile, odd rows see their smallest scores there: within one warp some
+def test_max_jumps_in_some_rows_only(fa, d, causal, k_last):
+    # even rows see a score jump in the last key tile (see above for its
+    # size), odd rows see their smallest scores there: within one warp some
     # rows move their reference maximum and others keep it
     N = 777
     q, k, v = make_qkv(1, 2, N, d, seed=78, device=DEV)
@@ -117,7 +124,7 @@ def test_max_jumps_in_some_rows_only(fa, d, causal):
     sign[1::2] = -1.0
     q = (q.float().abs() * sign[None, None, :, None]).to(torch.bfloat16)
     k = k.clone()
-    k[:, :, N - 5:, :] = 1.5
+    k[:, :, N - 5:, :] = k_last
     o, lse = run(fa, q, k, v, causal, d ** -0.5)
     assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "jump-some")
 
