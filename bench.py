@@ -250,6 +250,34 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def time_workload(fa, w, dev, steps, warmup, flush, peak_burst, sms, mhz):
+    """Median ms per mask of one fa_fwd call on workload w (L2 flushed before
+    each call, outside the events), with its fractions of the peaks."""
+    q, k, v = make_qkv(w.B, w.H, w.N, w.d, seed=4321, values=w.values, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+    out = {}
+    for causal in [c for c in (False, True) if c in w.causal]:
+        for _ in range(warmup):
+            fa.fa_fwd(q, k, v, o, lse, causal=causal, scale=w.scale)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fa.fa_fwd(q, k, v, o, lse, causal=causal, scale=w.scale)
+            e1.record()
+        torch.cuda.synchronize(dev)
+        ms = median([a.elapsed_time(b) for a, b in evs])
+        tf = flops(w, causal) / (ms * 1e-3) / 1e12
+        clock_peak = sms * TC_FLOP_PER_CLK_SM * mhz * 1e6 / 1e12 if mhz else None
+        out["causal" if causal else "non-causal"] = {
+            "ms": ms, "tflops": tf, "frac_of_measured_peak": tf / peak_burst,
+            "frac_of_clock_peak": tf / clock_peak if clock_peak else None,
+            "frac_of_spec_peak": tf / SPEC_BF16_TFLOPS}
+    del q, k, v, o, lse
+    return out
+
+
 def run_ours(args):
     from exact_attention_20_gb300 import build as fa_build
 
@@ -374,6 +402,16 @@ def run_ours(args):
             "frac_of_clock_peak": tf / clock_peak if clock_peak else None,
             "frac_of_spec_peak": tf / SPEC_BF16_TFLOPS}
 
+    # the other configurations of the method (parity cases; reported beside
+    # the headline, not part of its value), same protocol, after the timed
+    # region and its clock samples
+    others = {}
+    if world == 1 and not args.no_other_workloads:
+        for name, ow in WORKLOADS.items():
+            if name == w.name:
+                continue
+            others[name] = time_workload(fa, ow, dev, max(10, min(args.steps, 50)), 3, flush, peak_burst, sms, mhz)
+
     cpu = None
     if not args.no_cpu_baseline:
         rate, dt, desc = oracle_sample_rate(w, cpu_sample_heads(w, args.cpu_heads))
@@ -403,6 +441,7 @@ def run_ours(args):
                      "kernel": f"fa_fwd_kernel<{w.d},{str(masks[dom]).lower()}>",
                      "timed_span": "one fa_fwd call = one launch of this kernel (split items merged inside it)",
                      "traffic": recorded_traffic(w.name, masks[dom])},
+        "other_workloads": others or None,
         "cpu_baseline": cpu,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -632,6 +671,8 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=None,
                     help="heads of the oracle's CPU sample (default: about 100 GFLOP of work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the other configurations after the headline")
     ap.add_argument("--decode", action="store_true",
                     help="the few-query-rows shapes through fa_fwd_rect (HBM-bound), "
                          "instead of the headline step")
