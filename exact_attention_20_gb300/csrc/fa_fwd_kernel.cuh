@@ -254,6 +254,39 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
+// Steps before a chunk's end at which the next chunk's first tiles are
+// prefetched into L2 (the producer runs about half the ring ahead of the
+// tensor core, so this is several steps of work before they are needed).
+constexpr int kPrefetchSteps = 2;
+
+// L2 prefetch of chunk q's Q tiles and its first step's K and V tiles
+// (boxes past the end of a tensor are not fetched).
+template <int D, bool CAUSAL, int E, bool PAIRED>
+__device__ __forceinline__ void prefetch_chunk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                               int q, const WorkRange& wr, const SlotPair& sp, const FwdParams& p) {
+  using C = Cfg<D, E>;
+  const int item = chunk_item(q, wr);
+  int rb, bh;
+  decode_item(item, p, rb, bh);
+  const Chunk ch = chunk_of(item, item_steps<CAUSAL, PAIRED>(rb, p), wr, sp, p);
+  for (int t = 0; t < kQTiles; ++t) {
+    if (min(ch.ke, tiles_for<CAUSAL, PAIRED>(rb, t, p)) <= ch.kb) continue;
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmQ, s * (128 / E), tile_row0(rb, t, PAIRED), tile_head(bh, t, PAIRED));
+  }
+  for (int h = 0; h < (PAIRED ? 2 : 1); ++h) {
+    const int head = PAIRED ? 2 * bh + h : bh;
+#pragma unroll
+    for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmK, s * (128 / E), ch.kb * kBlockN, head);
+    if (E == 1) {
+      tma_prefetch_3d(tmV, ch.kb * kBlockN, 0, head);
+    } else {
+#pragma unroll
+      for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmV, s * (128 / E), ch.kb * kBlockN, head);
+    }
+  }
+}
+
 template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              uint32_t sbase, const Sync& sy, const FwdParams& p) {
@@ -300,7 +333,12 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
     if (p.starve_kv) continue;  // self-test: never deliver K/V
     // per step: K then V (normal), or K of both heads then V of both (paired)
     const int heads = PAIRED ? 2 : 1;
+    // A few steps before the chunk ends (at its start if it is short), the
+    // next chunk's Q tiles and first K, V tiles are brought into L2, so that
+    // their loads at the boundary are not DRAM round trips.
+    const int j_prefetch = max(ch.kb, ch.ke - kPrefetchSteps);
     for (int j = ch.kb; j < ch.ke && ok; ++j) {
+      if (j == j_prefetch && q + 1 < nq) prefetch_chunk<D, CAUSAL, E, PAIRED>(tmQ, tmK, tmV, q + 1, wr, sp, p);
 #pragma unroll
       for (int n = 0; n < 2 * heads; ++n) {
         if (!ok) break;
@@ -538,6 +576,16 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
 
 constexpr int kMaxPartsPerItem = 8;  // the plan splits no item into more parts
 
+// Workspace slot layout: a slot holds one part of an item, 256 rows of D
+// fp32 values, stored as D / 8 groups of eight columns, each group with its
+// 256 rows one after the other (32 bytes a row).  A thread owns a row (as in
+// tensor memory), so a warp's 32-byte access to one group covers 1 KB of
+// consecutive memory instead of 32 rows' separate sectors.
+template <int D>
+__device__ __forceinline__ size_t part_index(int slot, int row_in_item, int group) {
+  return (static_cast<size_t>(slot) * kItemRows * D) + (static_cast<size_t>(group) * kItemRows + row_in_item) * 8;
+}
+
 // A warp publishes its 32 rows of one part of a split item: O normalised over
 // the part's keys (the accumulator scaled by inv_l) in fp32, and the part's
 // natural-log logsumexp.  An empty part (no key of the chunk lies at or below
@@ -548,9 +596,8 @@ __device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_
                                              float inv_l, float lse_part, bool empty,
                                              const FwdParams& p) {
   const size_t prow = static_cast<size_t>(ch.slot) * kItemRows + t * kBlockM + row_in_tile;
+  const int r = t * kBlockM + row_in_tile;
   if (!empty) {
-    // workspace rows are D * 4 bytes in 256-byte aligned slots: 32-byte stores
-    float* dst = p.part_o + prow * D;
     const uint64_t il2 = f2_pack(inv_l, inv_l);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -564,7 +611,7 @@ __device__ __forceinline__ void publish_part(const Chunk& ch, int t, int row_in_
         o[2 * i + 1] = __float_as_uint(b);
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) st_global_v8(dst + c * 32 + i * 8, o + i * 8);
+      for (int i = 0; i < 4; ++i) st_global_v8(p.part_o + part_index<D>(ch.slot, r, c * 4 + i), o + i * 8);
     }
   }
   p.part_lse[prow] = lse_part;
@@ -579,55 +626,78 @@ constexpr int kNumCounters = kMaxCtas * kCountersPerItem;  // workspace counters
 // those 32 rows when its CTA's own work is done, reading its own part from
 // tensor memory when it is still there (the CTA's last chunk: nothing later
 // overwrites that O), and the other parts from the workspace.  In the last
-// chunk a warp first looks at the counter: if every other part is already
-// in, it is the last and publishes nothing.  No warp ever waits for
+// chunk every lane of a warp first reads the counter: if every other part is
+// already in, the warp is the last and publishes nothing.  A part in the
+// CTA's first chunk (its range starts inside an item) is published with
+// plain stores and its arrival is deferred: the warp makes it (a fence, then
+// the increment) at the start of its next chunk, while that chunk's first
+// scores are on their way, and looks at the increment's old value, which
+// says whether it merges, only after the last chunk.  No warp ever waits for
 // another CTA; the merging warp resets the counter for the next launch.
 struct PartSlots {
   int n;                       // parts of the item
   int slot[kMaxPartsPerItem];  // their workspace slots
 };
 
+constexpr int kInTmem = 1;    // this warp's part is still in tensor memory
+constexpr int kOwnEmpty = 2;  // this warp's part has no key for these rows (L = -inf, no O)
+constexpr int kAcquired = 4;  // every lane has read the counter with acquire and seen all other parts in
+
 struct PendingMerge {
   int k;          // split item, or -1 for none
   int own_slot;   // this warp's part's workspace slot (read from there unless in TMEM)
-  bool in_tmem;   // this warp's part is still in tensor memory
-  bool own_empty; // this warp's part has no key for these rows (L = -inf, no O)
+  int flags;      // kInTmem | kOwnEmpty | kAcquired
   float inv_l;    // 1 / lq of the own part (the accumulator -> normalised O)
   float lse_own;  // natural-log logsumexp of the own part
   int rb, bh;
 };
 
-template <int D>
-__device__ __forceinline__ PendingMerge part_done(const Chunk& ch, int t, int quad, int lane,
-                                                  int row_in_tile, uint32_t tO, float inv_l,
-                                                  float lse_part, bool empty, const FwdParams& p) {
-  int* ctr = p.counters + ch.k * kCountersPerItem + t * 4 + quad;
-  const int count = p.merge_count[ch.k];
-  PendingMerge pm{-1, ch.slot, ch.last, empty, inv_l, lse_part, ch.rb, ch.bh};
-  if (ch.last) {
-    int seen = 0;
-    if (lane == 0) seen = ld_acquire_gpu(ctr);
-    seen = __shfl_sync(0xffffffffu, seen, 0);
-    if (seen == count - 1) {  // every other part is in: merge, publish nothing
-      pm.k = ch.k;
-      return pm;
-    }
-  }
-  publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_part, empty, p);
+// The warp's arrival on a part counter, once its part's rows are stored:
+// returns the counter's old value in lane 0 (0 in the other lanes).
+__device__ __forceinline__ int part_arrive(int* ctr, int lane) {
   __threadfence();
   __syncwarp();
   int old = 0;
   if (lane == 0) old = atomicAdd(ctr, 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == count - 1) pm.k = ch.k;  // arrived last after all
+  return old;
+}
+
+// End of a chunk that is a part of its item.  Sets `arrival` to -1 when the
+// part is stored and its arrival is left to the caller (the CTA's first chunk).
+template <int D>
+__device__ __forceinline__ PendingMerge part_done(const Chunk& ch, int t, int quad, int lane,
+                                                  int row_in_tile, uint32_t tO, float inv_l,
+                                                  float lse_part, bool empty, int& arrival, const FwdParams& p) {
+  int* ctr = p.counters + ch.k * kCountersPerItem + t * 4 + quad;
+  const int count = p.merge_count[ch.k];
+  PendingMerge pm{-1, ch.slot, (ch.last ? kInTmem : 0) | (empty ? kOwnEmpty : 0), inv_l, lse_part, ch.rb, ch.bh};
+  if (ch.last) {
+    // every lane acquires: the other parts' rows were stored and fenced before
+    // their arrivals were counted
+    if (__all_sync(0xffffffffu, ld_acquire_gpu(ctr) == count - 1)) {  // merge, publish nothing
+      pm.k = ch.k;
+      pm.flags |= kAcquired;
+      return pm;
+    }
+  }
+  publish_part<D>(ch, t, row_in_tile, tO, inv_l, lse_part, empty, p);
+  if (!ch.last) {  // the arrival is left to the caller
+    pm.k = ch.k;
+    arrival = -1;
+    return pm;
+  }
+  if (__shfl_sync(0xffffffffu, part_arrive(ctr, lane), 0) == count - 1) pm.k = ch.k;  // arrived last after all
   return pm;
 }
 
 // Merges one warp's 32 rows (thread = row, as in tensor memory) of a split
 // item: L = ln sum_r exp(L_r), O = sum_r exp(L_r - L) O_r, the largest L_r
-// subtracted first; parts with L_r = -inf weigh 0 and are not read.  The own
-// part comes from tensor memory or its slot; the others from their slots,
-// 32 bytes per load.  Writes the final bf16 O and L of rows < Nq.
+// subtracted first; parts with L_r = -inf weigh 0 and their O is not used.
+// The own part comes from tensor memory or its slot, the others from their
+// slots.  With two parts (the usual case) the other part's logsumexp and its
+// first 32 columns are loaded together, and each next 32 columns while the
+// current ones are combined; with more parts each part's 32 columns are
+// loaded in turn.  Writes the final bf16 O and L of rows < Nq.
 template <int D>
 __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlots ps, int t, int quad,
                                         uint32_t tO, int* ctr, __nv_bfloat16* __restrict__ o,
@@ -637,86 +707,126 @@ __device__ __forceinline__ void merge_rows(const PendingMerge pm, const PartSlot
   const int r = t * kBlockM + quad * 32 + lane;  // row within the item (and its slot)
   const int row = tile_row0(pm.rb, t, paired) + quad * 32 + lane;
   const int head = tile_head(pm.bh, t, paired);
-  // Every lane acquires the counter itself: the other parts' rows were
-  // published (and fenced) before their arrivals were counted.  Then it is
-  // reset for the next launch: every arrival for these rows has happened.
-  (void)ld_acquire_gpu(ctr);
+  // Every lane acquires the counter itself (unless it already did), then it
+  // is reset for the next launch: every arrival for these rows has happened.
+  if (!(pm.flags & kAcquired)) (void)ld_acquire_gpu(ctr);
   __syncwarp();
   if (lane == 0) *ctr = 0;
-  // the other parts' logsumexps (the own part's is pm.lse_own)
-  float lr[kMaxPartsPerItem];
-  float m = pm.lse_own;
-#pragma unroll
-  for (int q = 0; q < kMaxPartsPerItem; ++q) {
-    const bool is_other = q < ps.n && ps.slot[q] != pm.own_slot;
-    lr[q] = is_other ? __ldcg(part_lse + static_cast<size_t>(ps.slot[q]) * kItemRows + r) : -INFINITY;
-    m = fmaxf(m, lr[q]);
-  }
+  const bool in_tmem = pm.flags & kInTmem;
+  const bool own_empty = pm.flags & kOwnEmpty;
   constexpr float kLog2e = 1.4426950408889634f;
-  const float w_own = pm.lse_own == -INFINITY ? 0.f : exp2f((pm.lse_own - m) * kLog2e);
-  float wsum = w_own;
-  float w[kMaxPartsPerItem];
-#pragma unroll
-  for (int q = 0; q < kMaxPartsPerItem; ++q) {
-    w[q] = lr[q] == -INFINITY ? 0.f : exp2f((lr[q] - m) * kLog2e);
-    wsum += w[q];
-  }
-  const float inv_w = 1.f / wsum;
   const bool store = row < Nq;
   __nv_bfloat16* orow = o + (static_cast<size_t>(head) * Nq + (store ? row : 0)) * D;
   const bool wide = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
-  const float* own_row = part_o + (static_cast<size_t>(pm.own_slot) * kItemRows + r) * D;
-  const float f_own = pm.in_tmem ? w_own * pm.inv_l * inv_w : w_own * inv_w;
-  // 64 columns at a time, each part's loads of them in flight together
-  constexpr int kHalf = D < 64 ? D : 64;
-#pragma unroll 1
-  for (int h = 0; h < D / kHalf; ++h) {
-    float acc[kHalf];
-    if (pm.own_empty) {
+  // the own part's 32 columns c0.., times f
+  auto own_cols = [&](int c0, float f, float* acc) {
+    if (own_empty) {
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) acc[i] = 0.f;
-    } else if (pm.in_tmem) {
+      for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    } else if (in_tmem) {
+      uint32_t x[32];
+      tmem_ld32_wait(tO + c0, x);
 #pragma unroll
-      for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t x[32];
-        tmem_ld32_wait(tO + h * kHalf + c * 32, x);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __uint_as_float(x[i]) * f_own;
-      }
+      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(x[i]) * f;
     } else {
 #pragma unroll
-      for (int i = 0; i < kHalf / 8; ++i) ld_global_cg_v8(own_row + h * kHalf + i * 8, acc + i * 8);
+      for (int i = 0; i < 4; ++i) ld_global_cg_v8(part_o + part_index<D>(pm.own_slot, r, c0 / 8 + i), acc + i * 8);
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) acc[i] *= f_own;
+      for (int i = 0; i < 32; ++i) acc[i] *= f;
     }
+  };
+  auto store_cols = [&](int c0, const float* acc) {
+    uint32_t pk[16];
 #pragma unroll
-    for (int q = 0; q < kMaxPartsPerItem; ++q) {
-      if (w[q] != 0.f) {  // weight 0: never written, never read
-        const float* src = part_o + (static_cast<size_t>(ps.slot[q]) * kItemRows + r) * D + h * kHalf;
-        float x[kHalf];
-#pragma unroll
-        for (int i = 0; i < kHalf / 8; ++i) ld_global_cg_v8(src + i * 8, x + i * 8);
-        const float wq = w[q] * inv_w;
-#pragma unroll
-        for (int i = 0; i < kHalf; ++i) acc[i] += wq * x[i];
-      }
-    }
-    uint32_t pk[kHalf / 2];
-#pragma unroll
-    for (int i = 0; i < kHalf / 2; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
     if (store) {
-      __nv_bfloat16* dst = orow + h * kHalf;
+      __nv_bfloat16* dst = orow + c0;
       if (wide) {
-#pragma unroll
-        for (int i = 0; i < kHalf / 16; ++i) st_global_v8(dst + i * 16, pk + i * 8);
+        st_global_v8(dst, pk);
+        st_global_v8(dst + 16, pk + 8);
       } else {
 #pragma unroll
-        for (int i = 0; i < kHalf / 8; ++i)
+        for (int i = 0; i < 4; ++i)
           reinterpret_cast<uint4*>(dst)[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
       }
     }
+  };
+  float lse_out;
+  if (ps.n == 2) {
+    const int s1 = ps.slot[0] == pm.own_slot ? ps.slot[1] : ps.slot[0];  // the other part
+    // 32 columns of the other part at a time, the next ones in flight while
+    // the current ones are combined (an empty part's rows were never
+    // written: loaded, then given weight 0)
+    float xa[32], xb[32];
+    const float l1 = __ldcg(part_lse + static_cast<size_t>(s1) * kItemRows + r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld_global_cg_v8(part_o + part_index<D>(s1, r, i), xa + i * 8);
+    const float m = fmaxf(pm.lse_own, l1);
+    const float w_own = own_empty ? 0.f : exp2f((pm.lse_own - m) * kLog2e);
+    const float w1 = l1 == -INFINITY ? 0.f : exp2f((l1 - m) * kLog2e);
+    const float wsum = w_own + w1;
+    const float inv_w = 1.f / wsum;
+    const float f_own = (in_tmem ? w_own * pm.inv_l : w_own) * inv_w;
+    const float f1 = w1 * inv_w;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float* cur = (c & 1) ? xb : xa;
+      float* nxt = (c & 1) ? xa : xb;
+      if (c + 1 < D / 32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_global_cg_v8(part_o + part_index<D>(s1, r, (c + 1) * 4 + i), nxt + i * 8);
+      }
+      float acc[32];
+      own_cols(c * 32, f_own, acc);
+      if (w1 != 0.f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] += f1 * cur[i];
+      }
+      store_cols(c * 32, acc);
+    }
+    lse_out = m + logf(wsum);
+  } else {
+    // three parts or more: the largest logsumexp, the weights' sum, then 32
+    // columns at a time with each other part's columns loaded in turn
+    float m = pm.lse_own;
+#pragma unroll 1
+    for (int q = 0; q < ps.n; ++q) {
+      const int sq = ps.slot[q];
+      if (sq != pm.own_slot) m = fmaxf(m, __ldcg(part_lse + static_cast<size_t>(sq) * kItemRows + r));
+    }
+    const float w_own = own_empty ? 0.f : exp2f((pm.lse_own - m) * kLog2e);
+    float wsum = w_own;
+#pragma unroll 1
+    for (int q = 0; q < ps.n; ++q) {
+      const int sq = ps.slot[q];
+      if (sq == pm.own_slot) continue;
+      const float lq = __ldcg(part_lse + static_cast<size_t>(sq) * kItemRows + r);
+      wsum += lq == -INFINITY ? 0.f : exp2f((lq - m) * kLog2e);
+    }
+    const float inv_w = 1.f / wsum;
+    const float f_own = (in_tmem ? w_own * pm.inv_l : w_own) * inv_w;
+#pragma unroll 1
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      float acc[32];
+      own_cols(c0, f_own, acc);
+#pragma unroll 1
+      for (int q = 0; q < ps.n; ++q) {
+        const int sq = ps.slot[q];
+        if (sq == pm.own_slot) continue;
+        const float lq = __ldcg(part_lse + static_cast<size_t>(sq) * kItemRows + r);
+        if (lq == -INFINITY) continue;  // never written, never read
+        const float wq = exp2f((lq - m) * kLog2e) * inv_w;
+        float x[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ld_global_cg_v8(part_o + part_index<D>(sq, r, c0 / 8 + i), x + i * 8);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] += wq * x[i];
+      }
+      store_cols(c0, acc);
+    }
+    lse_out = m + logf(wsum);
   }
-  if (store) lse[static_cast<size_t>(head) * Nq + row] = m + logf(wsum);
+  if (store) lse[static_cast<size_t>(head) * Nq + row] = lse_out;
 }
 
 // ---------------------------------------------------------------------------
@@ -741,7 +851,8 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   uint32_t s_par = 0;
   uint32_t od_par = 0;  // o_done completes once per chunk in which this tile has keys
   // split items this warp's rows complete, merged after the last chunk
-  PendingMerge pend0{-1, 0, false, false, 0.f, 0.f, 0, 0}, pend1 = pend0;
+  PendingMerge pend0{-1, 0, 0, 0.f, 0.f, 0, 0}, pend1 = pend0;
+  int arrival = -2;  // the first chunk's part: -2 none, -1 stored (arrival due), >= 0 arrived (lane 0: old value)
   bool ok = true;
 
   const WorkRange wr = p.range[blockIdx.x];
@@ -755,6 +866,9 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
     const int n = tiles_for<CAUSAL, PAIRED>(rb, t, p);       // key tiles of this query tile in the item
     const int ne = min(ch.ke, n);                    // ... and its part in this chunk: [kb, ne)
     const int row = tile_row0(rb, t, PAIRED) + row_in_tile;
+    // the first chunk's part: its arrival is made while this chunk's first
+    // scores are on their way
+    if (arrival == -1) arrival = part_arrive(p.counters + sp.k_first * kCountersPerItem + t * 4 + quad, lane);
     // FP8 path: this query tile's scale (one per 128 query rows)
     const float sq = E == 1 ? p.q_scale[static_cast<size_t>(bh) * ((p.Nq + kBlockM - 1) / kBlockM) +
                                         tile_row0(rb, t, PAIRED) / kBlockM]
@@ -763,7 +877,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       // No key tile of this query tile lies in the chunk (past its diagonal).
       // A part still reports its rows, as an empty part: LSE = -inf.
       if (ch.slot >= 0) {
-        const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, 0.f, -INFINITY, true, p);
+        const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, 0.f, -INFINITY, true, arrival, p);
         if (ch.todo) pend1 = pm; else pend0 = pm;
       }
       continue;
@@ -990,7 +1104,7 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
       if (store) p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse_row;
     } else {
       // a part of the item: merged once every part is in (merge_item)
-      const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, inv_l, lse_row, false, p);
+      const PendingMerge pm = part_done<D>(ch, t, quad, lane, row_in_tile, tO, inv_l, lse_row, false, arrival, p);
       if (ch.todo) pend1 = pm; else pend0 = pm;
     }
     tc_fence_before_sync();
@@ -1000,6 +1114,9 @@ __device__ __forceinline__ void run_softmax(int t, uint32_t tmem, const Sync& sy
   // The merges of the split items these rows completed.  The last chunk's O
   // is still in tensor memory: no product of this tile follows it.
   if (!ok || *sy.abort_flag) return;
+  // the first chunk's part, when no later chunk of this tile made its arrival
+  if (arrival == -1) arrival = part_arrive(p.counters + sp.k_first * kCountersPerItem + t * 4 + quad, lane);
+  if (arrival >= 0 && __shfl_sync(0xffffffffu, arrival, 0) != p.merge_count[sp.k_first] - 1) pend0.k = -1;
 #pragma unroll 1
   for (int i = 0; i < 2; ++i) {
     const PendingMerge pm = i ? pend1 : pend0;
