@@ -17,7 +17,7 @@
 // memory for the whole launch, and walks the query rows 64 at a time (a
 // step).  Every product is taken transposed so that the 128 keys are the
 // tensor-memory lanes and one thread owns one key row:
-//   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d (K read from TMEM)
+//   S^T  = K Q^T      M = 128 keys, N = 64 queries, K = d
 //   dP^T = V dO^T     same shape
 //   dV  += P^T dO     M = 128 keys, N = d, K = 64 queries (P^T read from TMEM)
 //   dK  += dS^T Q     same shape (dS^T read from TMEM)
@@ -29,27 +29,29 @@
 // still has M = 128: rows 64-127 of its A operand are V^T (the tile that
 // follows K in shared memory) and those lanes are ignored.
 //
-// The tensor core reads both operands of a product from shared memory unless
-// A comes from TMEM, and at M = 128 that read, not the arithmetic, sets the
-// pace of the N = 64 products and starves every other shared-memory access;
-// so K (the same for every step) and P^T and dS^T (made by the threads) are
-// handed to the tensor core in TMEM wherever they are an A operand.
-//
 // Warp roles (12 warps, 384 threads):
 //   warp 0     TMA producer: K and V once; Q, dO and their rows' L and D per step
-//   warp 1     MMA issuer (one lane issues), owner of the TMEM allocation
-//   warps 2-3  idle
-//   warps 4-7  K into TMEM once; P and dS, one key row per thread; the dK,
-//              dV epilogue
+//   warp 1     MMA issuer B (one lane issues): dV, dK, dQ^T; owner of the
+//              TMEM allocation
+//   warp 2     MMA issuer A (one lane issues): S^T, dP^T
+//   warp 3     idle
+//   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
 //   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread, reduced
 //              into the fp32 accumulator
-// Tensor memory (32-bit columns): K (bf16, two per column) at 0, S^T in two
-// buffers at 64 and 128, dP^T at 192, dV at 256, dK at 384.  P^T and dS^T
-// (bf16) overwrite the first and the second 32 columns of their S^T buffer;
-// S^T has two buffers so that the S^T of a later step is computed while this
-// step's P^T and dS^T still feed dV and dK.  dQ^T goes to dP^T's columns once
-// the threads have read dP^T, and the next dP^T waits until the drain has
-// read dQ^T.
+// Tensor memory (32-bit columns): S^T in two buffers at 0 and 64 (P^T and
+// dS^T, bf16, overwrite its first and second 32 columns), dP^T at 128, dQ^T
+// at 192, dV at 256, dK at 384; the dS^T tile in shared memory has two
+// buffers too.
+//
+// At M = 128 the tensor core takes an N = 64 instruction every 48 cycles and
+// accepts about one more than it is running, so an issuer that stops to wait
+// for a barrier leaves it idle; a product's result reaches the threads about
+// 220 cycles after its last instruction.  The products are therefore issued
+// by two warps, each waiting only for its own operands: issuer A computes
+// the threads' next operands (dP^T(it+1) as soon as the threads have read
+// dP^T(it), S^T(it+2) as soon as dK(it) has read its buffer), issuer B the
+// products of the threads' last step (dV(it), dK(it), dQ^T(it)).  While one
+// waits, the other's instructions keep the tensor core busy.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -63,14 +65,14 @@ constexpr int kBlockK = 128;   // keys per CTA
 constexpr int kBlockQ = 64;    // query rows per step
 constexpr int kThreads = 384;
 constexpr int kLoadWarp = 0;
-constexpr int kMmaWarp = 1;
+constexpr int kMmaWarp = 1;    // dV, dK, dQ^T; owns the tensor memory
+constexpr int kMmaWarpA = 2;   // S^T, dP^T
 constexpr int kDsWarp0 = 4;    // first warp of the P / dS warpgroup
 constexpr int kDrainWarp0 = 8; // first warp of the dQ drain warpgroup
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColK = 0;
-constexpr uint32_t kColS = 64;   // + 64 * buffer
-constexpr uint32_t kColDP = 192;
-constexpr uint32_t kColDQ = kColDP;
+constexpr uint32_t kColS = 0;    // S^T of step it at kColS + 64 * (it % 2); P^T, dS^T over it
+constexpr uint32_t kColDP = 128;
+constexpr uint32_t kColDQ = 192;
 constexpr uint32_t kColDV = 256;
 constexpr uint32_t kColDK = 384;
 
@@ -88,8 +90,8 @@ constexpr int kPrefetchSteps = 4;
 template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dimension 64 or 128");
-  // Q / dO ring depth: a step's tiles are requested three steps ahead.
-  static constexpr int kStages = 4;
+  // Q / dO ring depth: a step's tiles are requested two steps ahead.
+  static constexpr int kStages = 3;
   static constexpr int kKSlab = kBlockK * 128;  // 128 rows x 64 bf16 (one TMA box)
   static constexpr int kQSlab = kBlockQ * 128;  // 64 rows x 64 bf16
   static constexpr int kKTile = (D / 64) * kKSlab;
@@ -99,17 +101,17 @@ struct Cfg {
   static constexpr int kStageOff = kVOff + kKTile;
   static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries]
-  static constexpr int kLdOff = kDsOff + kDsBytes;        // per stage: L[64] then D[64], fp32
+  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries], two buffers
+  static constexpr int kLdOff = kDsOff + 2 * kDsBytes;    // per stage: L[64] then D[64], fp32
   static constexpr int kLdBytes = 2 * kBlockQ * 4;
   static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
-  static constexpr int kNumBars = 9 + 2 * kStages;
+  static constexpr int kNumBars = 14 + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
   // No alignment slack: the dynamic shared memory of a CTA starts on a
   // 1024-byte boundary (after the 1 KB the system reserves); the kernel checks
   // this and gives up (status word) if it ever does not.
   static constexpr int kSmemBytes = kMiscOff + 16;
-  static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStageBytes % 1024 == 0,
+  static_assert(kStageOff % 1024 == 0 && kDsOff % 1024 == 0 && kStageBytes % 1024 == 0 && kDsBytes % 1024 == 0,
                 "operand tiles must sit on 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
@@ -128,18 +130,30 @@ struct BwdParams {
   unsigned long long wait_limit_ns;
 };
 
-// Barrier addresses.  The pairs (one per stage or buffer) are adjacent, so
-// buffer b's barrier is the pair's address + 8 b (no run-time array index,
-// which would put the struct in local memory).
-// dq_full completes once per step, when that step's dQ^T product is done:
-// the drain then reads dQ^T, and the dS^T tile the product read may be
-// written again.
+// Barrier addresses.  Barriers that come in pairs (one per stage or buffer)
+// are adjacent, so the one of buffer b is the first one's address + 8 b (no
+// run-time array index, which would put the struct in local memory).
+//   s_full(b)   S^T of a step in buffer b (completes every other step)
+//   s_free(b)   dV and dK of a step have read buffer b (every other step)
+//   dp_full     dP^T of a step in tensor memory
+//   dp_read     the threads have read it: the next step's dP^T may go there
+//   sm_done(b)  the threads' P^T, dS^T of a step in buffer b are in tensor
+//               memory and its dS^T tile in shared memory (every other step)
+//   dq_full(b)  dQ^T of a step whose dS^T tile is buffer b is done: the drain
+//               reads it, and the tile may be written again (every other step)
+//   dq_free     the drain has read dQ^T
+// Every parity wait is safe by construction: the barrier's next completion
+// after the awaited one needs an action that comes after the wait.
 struct Sync {
-  uint32_t kv_full, k_ready, stage_full0, stage_empty0, s_full0, dp_full, sm_done, dq_full, dq_free, acc_done;
+  uint32_t kv_full, stage_full0, stage_empty0, s_full0, s_free0, dp_full, dp_read, sm_done0, dq_full0, dq_free,
+      acc_done, a_done;
   volatile int* abort_flag;
   __device__ __forceinline__ uint32_t stage_full(int b) const { return stage_full0 + 8 * b; }
   __device__ __forceinline__ uint32_t stage_empty(int b) const { return stage_empty0 + 8 * b; }
   __device__ __forceinline__ uint32_t s_full(int b) const { return s_full0 + 8 * b; }
+  __device__ __forceinline__ uint32_t s_free(int b) const { return s_free0 + 8 * b; }
+  __device__ __forceinline__ uint32_t sm_done(int b) const { return sm_done0 + 8 * b; }
+  __device__ __forceinline__ uint32_t dq_full(int b) const { return dq_full0 + 8 * b; }
 };
 
 // Bounded wait: true when the phase completed; false if this CTA is aborting
@@ -240,8 +254,9 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
 template <int D>
 struct Desc {
   using C = Cfg<D>;
-  uint64_t v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_mn0;
+  uint64_t k_kmaj, v_kmaj, kt_mn, q_kmaj0, do_kmaj0, q_mn0, do_mn0, ds_mn0;
   __device__ __forceinline__ explicit Desc(uint32_t sbase) {
+    k_kmaj = sdesc_sw128(sbase + C::kKOff, 16, 1024);
     v_kmaj = sdesc_sw128(sbase + C::kVOff, 16, 1024);
     kt_mn = sdesc_sw128(sbase + C::kKOff, C::kKSlab, 1024);
     const uint32_t st = sbase + C::kStageOff;
@@ -252,16 +267,17 @@ struct Desc {
     const uint32_t ds = sbase + C::kDsOff;
     ds_mn0 = sdesc_sw128(ds, C::kDsBytes, 1024);  // N = 64: one slab, the leading offset is not used
   }
+  __device__ __forceinline__ uint64_t ds_mn(int b) const { return sdesc_advance(ds_mn0, b * C::kDsBytes); }
   __device__ __forceinline__ uint64_t q_kmaj(int b) const { return sdesc_advance(q_kmaj0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t do_kmaj(int b) const { return sdesc_advance(do_kmaj0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t q_mn(int b) const { return sdesc_advance(q_mn0, b * C::kStageBytes); }
   __device__ __forceinline__ uint64_t do_mn(int b) const { return sdesc_advance(do_mn0, b * C::kStageBytes); }
 };
 
-// dP^T = V dO^T: A = the V tile (128 keys), B = the dO tile (64 rows), both
-// K-major over d in shared memory.
+// S^T = K Q^T and dP^T = V dO^T: A = the K or V tile (128 keys), B = the Q
+// or dO tile (64 rows), both K-major over d in shared memory.
 template <int D>
-__device__ __forceinline__ void issue_dp(uint32_t d_tmem, uint64_t a, uint64_t b) {
+__device__ __forceinline__ void issue_kmaj(uint32_t d_tmem, uint64_t a, uint64_t b) {
   using C = Cfg<D>;
   constexpr uint32_t idesc = idesc_bf16_f32_ab(kBlockK, kBlockQ, false, false);
 #pragma unroll
@@ -270,18 +286,64 @@ __device__ __forceinline__ void issue_dp(uint32_t d_tmem, uint64_t a, uint64_t b
             sdesc_advance(b, (kk / 4) * C::kQSlab + (kk % 4) * 32), idesc, kk > 0 ? 1u : 0u);
 }
 
-// S^T = K Q^T: A = K from tensor memory (16 values of d = 8 columns per
-// instruction), B = the Q tile, K-major over d in shared memory.
+// Issuer A: S^T and dP^T, the threads' operands.  Order:
+//   before the loop:  S^T(0)  dP^T(0)  S^T(1)
+//   step it:          [the threads have read dP^T(it)]  dP^T(it+1)
+//                     [dK(it) has read buffer it % 2]   S^T(it+2) into it
+// A stage is released by both issuers: by A after its dP^T, by B after its dK.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t k_tmem, uint64_t b) {
+__device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const Sync& sy, const BwdParams& p, int n) {
   using C = Cfg<D>;
-  constexpr uint32_t idesc = idesc_bf16_f32_ab(kBlockK, kBlockQ, false, false);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk)
-    umma_ts(d_tmem, k_tmem + kk * 8, sdesc_advance(b, (kk / 4) * C::kQSlab + (kk % 4) * 32), idesc,
-            kk > 0 ? 1u : 0u);
+  const bool leader = (threadIdx.x & 31) == 0;
+  bool ok = true;
+  auto wait_voted = [&](uint32_t bar, uint32_t par) {
+    ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
+  };
+  const Desc<D> ds(sbase);
+  wait_voted(sy.kv_full, 0);
+  auto issue_s_step = [&](int step) {  // S^T(step) into buffer step % 2, once its stage is in
+    wait_voted(sy.stage_full(step % C::kStages), (step / C::kStages) & 1);
+    if (!ok) return;
+    tc_fence_after_sync();
+    if (leader) {
+      issue_kmaj<D>(tmem + kColS + (step & 1) * 64, ds.k_kmaj, ds.q_kmaj(step % C::kStages));
+      umma_commit(sy.s_full(step & 1));
+    }
+    __syncwarp();
+  };
+  auto issue_dp_step = [&](int step) {  // dP^T(step) (its stage is in: S^T(step) read it)
+    tc_fence_after_sync();
+    if (leader) {
+      issue_kmaj<D>(tmem + kColDP, ds.v_kmaj, ds.do_kmaj(step % C::kStages));
+      umma_commit(sy.dp_full);
+      umma_commit(sy.stage_empty(step % C::kStages));  // A's last read of the stage
+    }
+    __syncwarp();
+  };
+  if (n > 0) {
+    issue_s_step(0);
+    if (ok) issue_dp_step(0);
+    if (n > 1 && ok) issue_s_step(1);
+  }
+  for (int it = 0; it < n && ok; ++it) {
+    if (it + 1 < n) {
+      wait_voted(sy.dp_read, it & 1);  // the threads have read dP^T(it)
+      if (!ok) break;
+      issue_dp_step(it + 1);
+    }
+    if (it + 2 < n) {
+      wait_voted(sy.s_free(it & 1), (it >> 1) & 1);  // dV(it), dK(it) have read buffer it % 2
+      if (!ok) break;
+      issue_s_step(it + 2);
+    }
+  }
+  if (leader) umma_commit(sy.a_done);
+  __syncwarp();
+  mbar_wait_bounded(sy.a_done, 0, p.wait_limit_ns);
 }
 
+// Issuer B: the products of the threads' step it, once its P^T and dS^T are
+// in: dV(it), dK(it), then dQ^T(it) once the drain has read dQ^T(it-1).
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy,
                                         const BwdParams& p, int n) {
@@ -292,96 +354,41 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
   };
   const Desc<D> ds(sbase);
-  const uint32_t tm_dp = tmem + kColDP, tm_dq = tmem + kColDQ;
+  const uint32_t tm_dq = tmem + kColDQ;
   const uint32_t tm_dv = tmem + kColDV, tm_dk = tmem + kColDK;
   constexpr uint32_t id_acc = idesc_bf16_f32_ab(kBlockK, D, false, true);      // dV, dK
   constexpr uint32_t id_dq = idesc_bf16_f32_ab(128, kBlockQ, true, true);      // dQ^T
-  // Order of the products (step it uses S^T buffer b = it % 2 and Q / dO
-  // stage it % kStages):
-  //   before the loop:  S^T(0), dP^T(0), S^T(1)
-  //   step it:          [P^T, dS^T of step it ready]  dQ^T(it)  dV(it)
-  //                     [drain has read dQ^T(it)]     dP^T(it+1)  dK(it)
-  //                     S^T(it+2) into buffer b
-  // dQ^T(it) overwrites dP^T(it), which the threads have read; dP^T(it+1) is
-  // what the threads wait on next, so it goes out as soon as the drain has
-  // emptied the columns, behind dV(it) which covers the drain's read.
   wait_voted(sy.kv_full, 0);
-  wait_voted(sy.k_ready, 0);  // K in tensor memory
-  auto stage_ready = [&](int step) {
-    wait_voted(sy.stage_full(step % C::kStages), (step / C::kStages) & 1);
-  };
-  if (n > 0 && ok) {
-    stage_ready(0);
-    if (ok) {
-      tc_fence_after_sync();
-      if (leader) {
-        issue_s<D>(tmem + kColS, tmem + kColK, ds.q_kmaj(0));
-        umma_commit(sy.s_full(0));
-        issue_dp<D>(tm_dp, ds.v_kmaj, ds.do_kmaj(0));
-        umma_commit(sy.dp_full);
-      }
-      __syncwarp();
-    }
-    if (n > 1 && ok) {
-      stage_ready(1);
-      if (ok) {
-        tc_fence_after_sync();
-        if (leader) {
-          issue_s<D>(tmem + kColS + 64, tmem + kColK, ds.q_kmaj(1));
-          umma_commit(sy.s_full(1));
-        }
-        __syncwarp();
-      }
-    }
-  }
   for (int it = 0; it < n && ok; ++it) {
-    const int b = it & 1;                 // S^T buffer (P^T, dS^T in TMEM)
-    const int st = it % C::kStages;       // Q / dO stage
+    const int st = it % C::kStages;
+    const int b = it & 1;
     const uint32_t tm_s = tmem + kColS + b * 64;
-    wait_voted(sy.sm_done, it & 1);  // P^T, dS^T in TMEM, dS^T in shared memory; S^T, dP^T read
+    wait_voted(sy.sm_done(b), (it >> 1) & 1);  // P^T, dS^T of step it in
     if (!ok) break;
     tc_fence_after_sync();
     const uint32_t acc = it > 0 ? 1u : 0u;
     if (leader) {
 #pragma unroll
-      for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T
-        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn0, kk * 2048), id_dq,
-                kk > 0 ? 1u : 0u);
-      umma_commit(sy.dq_full);
-#pragma unroll
       for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dV += P^T dO
         umma_ts(tm_dv, tm_s + kk * 8, sdesc_advance(ds.do_mn(st), kk * 2048), id_acc, kk > 0 ? 1u : acc);
-    }
-    __syncwarp();
-    if (it + 1 < n) {
-      wait_voted(sy.dq_free, it & 1);  // the drain has read dQ^T(it)
-      if (!ok) break;
-      tc_fence_after_sync();
-      if (leader) {
-        issue_dp<D>(tm_dp, ds.v_kmaj, ds.do_kmaj((it + 1) % C::kStages));
-        umma_commit(sy.dp_full);
-      }
-      __syncwarp();
-    }
-    if (leader) {
 #pragma unroll
       for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
         umma_ts(tm_dk, tm_s + 32 + kk * 8, sdesc_advance(ds.q_mn(st), kk * 2048), id_acc, kk > 0 ? 1u : acc);
-      umma_commit(sy.stage_empty(st));  // the step's Q and dO are no longer read
+      umma_commit(sy.s_free(b));
+      umma_commit(sy.stage_empty(st));  // B's last read of the stage
     }
     __syncwarp();
-    if (it + 2 < n) {
-      // S^T(it+2) into buffer b: P^T(it) and dS^T(it) there were read by
-      // dV(it) and dK(it), issued before it
-      stage_ready(it + 2);
-      if (!ok) break;
-      tc_fence_after_sync();
-      if (leader) {
-        issue_s<D>(tm_s, tmem + kColK, ds.q_kmaj((it + 2) % C::kStages));
-        umma_commit(sy.s_full(b));
-      }
-      __syncwarp();
+    if (it > 0) wait_voted(sy.dq_free, (it - 1) & 1);  // the drain has read dQ^T(it-1)
+    if (!ok) break;
+    tc_fence_after_sync();
+    if (leader) {
+#pragma unroll
+      for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T
+        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
+                kk > 0 ? 1u : 0u);
+      umma_commit(sy.dq_full(b));
     }
+    __syncwarp();
   }
   // Completes when every product issued above has: the epilogue's signal,
   // and the condition for releasing tensor memory.
@@ -405,32 +412,6 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   const uint64_t qk2 = f2_pack(p.qk_scale, p.qk_scale);
   bool ok = true;
-  {
-    // K of this thread's key row into tensor memory, the A operand of S^T:
-    // row r of the 128-byte-swizzled K tile (16-byte chunk c of a 64-column
-    // slab at chunk c ^ (r % 8)), two bf16 values of d per column.
-    ok = __all_sync(0xffffffffu, wait_phase(sy.kv_full, 0, sy, p, kSiteDs));
-    if (ok) {
-#pragma unroll
-      for (int sl = 0; sl < D / 64; ++sl) {
-        uint32_t kw[32];
-        const uint8_t* krow = smem + C::kKOff + sl * C::kKSlab + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(krow + ((c ^ (r & 7)) * 16));
-          kw[4 * c] = v.x;
-          kw[4 * c + 1] = v.y;
-          kw[4 * c + 2] = v.z;
-          kw[4 * c + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + kColK + sl * 32, kw);
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sy.k_ready);
-    }
-  }
   for (int it = 0; it < n && ok; ++it) {
     const int b = it & 1;
     const int st = it % C::kStages;
@@ -473,6 +454,7 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
       for (int c = 0; c < kBlockQ; ++c) pf[c] = c < cmin ? 0.f : pf[c];
     }
     {
+      // P^T over the first 32 columns of S^T (all of which are in registers)
       uint32_t pk[kBlockQ / 2];
 #pragma unroll
       for (int i = 0; i < kBlockQ / 2; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
@@ -481,29 +463,31 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
 
     // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16, stored to tensor
     // memory after P^T (the A operand of dK) and to the 128-byte-swizzled dS^T
-    // tile in shared memory (the B operand of dQ^T; 16-byte chunk ch of row r
-    // at chunk ch ^ (r % 8)).
+    // tile it % 2 in shared memory (the B operand of dQ^T; 16-byte chunk ch of
+    // row r at chunk ch ^ (r % 8)).
     w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
-    // The dS^T tile in shared memory was last read by dQ^T(it-1): wait for
-    // dq_full's completion of step it-1.  (A parity wait sees its phase only
-    // while the barrier is at most one completion past it; the completion of
-    // step it needs this warpgroup's step it, so it cannot have happened.)
-    if (it >= 1) w = w && wait_phase(sy.dq_full, (it - 1) & 1, sy, p, kSiteDs);
+    // Tile it % 2 was last read by dQ^T(it-2): wait for that completion of
+    // its barrier (the next one, step it's, needs this warpgroup's step it).
+    if (it >= 2) w = w && wait_phase(sy.dq_full(b), ((it - 2) >> 1) & 1, sy, p, kSiteDs);
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after_sync();
-    uint8_t* ds_row = smem + C::kDsOff + r * 128;
+    uint32_t dpt[kBlockQ];
+    tmem_ld64_wait(tmem + lane_off + kColDP, dpt);
+    // dP^T is in registers: the next step's dP^T may take its columns
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sy.dp_read);
+    uint8_t* ds_row = smem + C::kDsOff + b * C::kDsBytes + r * 128;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      uint32_t d32[32];
-      tmem_ld32_wait(tmem + lane_off + kColDP + h * 32, d32);
       uint32_t wds[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = h * 32 + 2 * i;
         const float2 dd = *reinterpret_cast<const float2*>(Drow + c);
-        const float g0 = pf[c] * (__uint_as_float(d32[2 * i]) - dd.x);
-        const float g1 = pf[c + 1] * (__uint_as_float(d32[2 * i + 1]) - dd.y);
+        const float g0 = pf[c] * (__uint_as_float(dpt[c]) - dd.x);
+        const float g1 = pf[c + 1] * (__uint_as_float(dpt[c + 1]) - dd.y);
         wds[i] = pack_bf16x2(g0, g1);
       }
 #pragma unroll
@@ -518,7 +502,7 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
     fence_proxy_async_smem();  // dS^T is visible to the tensor core
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(sy.sm_done);
+    if (lane == 0) mbar_arrive(sy.sm_done(b));
   }
 
   // Epilogue: dV and scale * dK of this thread's key row, bf16.  A block with
@@ -572,7 +556,7 @@ __device__ __forceinline__ void run_drain(uint32_t tmem, const Sync& sy, const B
   const bool has_rows = quad * 32 < D;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   for (int it = 0; it < n; ++it) {
-    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full, it & 1, sy, p, kSiteDrain));
+    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full(it & 1), (it >> 1) & 1, sy, p, kSiteDrain));
     if (!ok) break;
     tc_fence_after_sync();
     uint32_t x[kBlockQ];
@@ -625,35 +609,44 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint32_t b = sbase + C::kBarOff;
     auto next = [&]() { const uint32_t r = b; b += 8; return r; };
     sy.kv_full = next();
-    sy.k_ready = next();
     sy.stage_full0 = next();
     for (int i = 1; i < C::kStages; ++i) next();
     sy.stage_empty0 = next();
     for (int i = 1; i < C::kStages; ++i) next();
     sy.s_full0 = next();
     next();
+    sy.s_free0 = next();
+    next();
     sy.dp_full = next();
-    sy.sm_done = next();
-    sy.dq_full = next();
+    sy.dp_read = next();
+    sy.sm_done0 = next();
+    next();
+    sy.dq_full0 = next();
+    next();
     sy.dq_free = next();
     sy.acc_done = next();
+    sy.a_done = next();
   }
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMiscOff);
   sy.abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
 
   if (threadIdx.x == 0) {
     mbar_init(sy.kv_full, 1);
-    mbar_init(sy.k_ready, 4);  // one arrival per P / dS warp
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(sy.stage_full(i), 1);
-      mbar_init(sy.stage_empty(i), 1);
+      mbar_init(sy.stage_empty(i), 2);  // released by both issuers
     }
-    for (int i = 0; i < 2; ++i) mbar_init(sy.s_full(i), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sy.s_full(i), 1);
+      mbar_init(sy.s_free(i), 1);
+      mbar_init(sy.sm_done(i), 4);  // one arrival per P / dS warp
+      mbar_init(sy.dq_full(i), 1);
+    }
     mbar_init(sy.dp_full, 1);
-    mbar_init(sy.sm_done, 4);  // one arrival per P / dS warp
-    mbar_init(sy.dq_full, 1);
+    mbar_init(sy.dp_read, 4);  // one arrival per P / dS warp
     mbar_init(sy.dq_free, 4);  // one arrival per drain warp
     mbar_init(sy.acc_done, 1);
+    mbar_init(sy.a_done, 1);
     *sy.abort_flag = 0;
     fence_barrier_init();
   }
@@ -677,6 +670,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncwarp();
   } else if (warp == kMmaWarp) {
     run_mma<D, CAUSAL>(sbase, tmem, sy, p, n);
+  } else if (warp == kMmaWarpA) {
+    run_mma_a<D>(sbase, tmem, sy, p, n);
   } else if (warp >= kDsWarp0 && warp < kDsWarp0 + 4) {
     run_ds<D, CAUSAL>(smem, tmem, sy, p, bh, kb, j0, n);
   } else if (warp >= kDrainWarp0) {
