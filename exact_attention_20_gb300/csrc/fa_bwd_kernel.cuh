@@ -38,10 +38,13 @@
 //   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
 //   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread, reduced
 //              into the fp32 accumulator
-// Tensor memory (32-bit columns): S^T in two buffers at 0 and 64 (P^T and
-// dS^T, bf16, overwrite its first and second 32 columns), dP^T at 128, dQ^T
-// at 192, dV at 256, dK at 384; the dS^T tile in shared memory has two
-// buffers too.
+// Tensor memory (32-bit columns): three 64-column buffers at 0, 64 and 128,
+// one per step in turn: a step's S^T, then its P^T and dS^T (bf16, the
+// first and the second 32 columns, written over S^T by the threads), then
+// its dQ^T (written once dV and dK have read P^T and dS^T); dP^T at 192, dV
+// at 256, dK at 384.  The dS^T tile in shared memory has three buffers too.
+// A buffer takes S^T again once the drain has read its dQ^T, so S^T runs up
+// to three steps ahead of the threads.
 //
 // At M = 128 the tensor core takes an N = 64 instruction every 48 cycles and
 // accepts about one more than it is running, so an issuer that stops to wait
@@ -49,9 +52,10 @@
 // 220 cycles after its last instruction.  The products are therefore issued
 // by two warps, each waiting only for its own operands: issuer A computes
 // the threads' next operands (dP^T(it+1) as soon as the threads have read
-// dP^T(it), S^T(it+2) as soon as dK(it) has read its buffer), issuer B the
-// products of the threads' last step (dV(it), dK(it), dQ^T(it)).  While one
-// waits, the other's instructions keep the tensor core busy.
+// dP^T(it), S^T(it+2) as soon as the drain has read dQ^T(it-1) from its
+// buffer), issuer B the products of the threads' last step (dV(it), dK(it),
+// dQ^T(it)).  While one waits, the other's instructions keep the tensor core
+// busy.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -70,9 +74,10 @@ constexpr int kMmaWarpA = 2;   // S^T, dP^T
 constexpr int kDsWarp0 = 4;    // first warp of the P / dS warpgroup
 constexpr int kDrainWarp0 = 8; // first warp of the dQ drain warpgroup
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;    // S^T of step it at kColS + 64 * (it % 2); P^T, dS^T over it
-constexpr uint32_t kColDP = 128;
-constexpr uint32_t kColDQ = 192;
+constexpr int kSBufs = 3;        // S^T buffers (and dS^T tiles in shared memory)
+constexpr uint32_t kColS = 0;    // buffer of step it at kColS + 64 * (it % kSBufs): S^T, then P^T and
+                                 // dS^T over it, then dQ^T
+constexpr uint32_t kColDP = 192;
 constexpr uint32_t kColDV = 256;
 constexpr uint32_t kColDK = 384;
 
@@ -101,11 +106,11 @@ struct Cfg {
   static constexpr int kStageOff = kVOff + kKTile;
   static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries], two buffers
-  static constexpr int kLdOff = kDsOff + 2 * kDsBytes;    // per stage: L[64] then D[64], fp32
+  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries], kSBufs tiles
+  static constexpr int kLdOff = kDsOff + kSBufs * kDsBytes;  // per stage: L[64] then D[64], fp32
   static constexpr int kLdBytes = 2 * kBlockQ * 4;
   static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
-  static constexpr int kNumBars = 14 + 2 * kStages;
+  static constexpr int kNumBars = 11 + 4 * kSBufs + 2 * kStages;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
   // No alignment slack: the dynamic shared memory of a CTA starts on a
   // 1024-byte boundary (after the 1 KB the system reserves); the kernel checks
@@ -130,31 +135,38 @@ struct BwdParams {
   unsigned long long wait_limit_ns;
 };
 
-// Barrier addresses.  Barriers that come in pairs (one per stage or buffer)
+// Barrier addresses.  Barriers that come in sets (one per stage or buffer)
 // are adjacent, so the one of buffer b is the first one's address + 8 b (no
 // run-time array index, which would put the struct in local memory).
-//   s_full(b)   S^T of a step in buffer b (completes every other step)
-//   s_free(b)   dV and dK of a step have read buffer b (every other step)
+// Buffer barriers complete once every kSBufs steps:
+//   s_full(b)   S^T of a step in buffer b
+//   sm_done(b)  the threads' P^T, dS^T of a step in buffer b are in, and its
+//               dS^T tile b in shared memory
+//   dq_full(b)  dQ^T of a step in buffer b: the drain reads it, and dS^T
+//               tile b may be written again
+//   dq_free(b)  the drain has read it: buffer b may take S^T again
+// and once per step:
 //   dp_full     dP^T of a step in tensor memory
 //   dp_read     the threads have read it: the next step's dP^T may go there
-//   sm_done(b)  the threads' P^T, dS^T of a step in buffer b are in tensor
-//               memory and its dS^T tile in shared memory (every other step)
-//   dq_full(b)  dQ^T of a step whose dS^T tile is buffer b is done: the drain
-//               reads it, and the tile may be written again (every other step)
-//   dq_free     the drain has read dQ^T
+//   stage_empty the step's products have read its Q / dO stage (one arrival
+//               from each issuer)
 // Every parity wait is safe by construction: the barrier's next completion
 // after the awaited one needs an action that comes after the wait.
 struct Sync {
-  uint32_t kv_full, stage_full0, stage_empty0, s_full0, s_free0, dp_full, dp_read, sm_done0, dq_full0, dq_free,
+  uint32_t kv_full, stage_full0, stage_empty0, s_full0, dp_full, dp_read, sm_done0, dq_full0, dq_free0,
       acc_done, a_done;
   volatile int* abort_flag;
   __device__ __forceinline__ uint32_t stage_full(int b) const { return stage_full0 + 8 * b; }
   __device__ __forceinline__ uint32_t stage_empty(int b) const { return stage_empty0 + 8 * b; }
   __device__ __forceinline__ uint32_t s_full(int b) const { return s_full0 + 8 * b; }
-  __device__ __forceinline__ uint32_t s_free(int b) const { return s_free0 + 8 * b; }
   __device__ __forceinline__ uint32_t sm_done(int b) const { return sm_done0 + 8 * b; }
   __device__ __forceinline__ uint32_t dq_full(int b) const { return dq_full0 + 8 * b; }
+  __device__ __forceinline__ uint32_t dq_free(int b) const { return dq_free0 + 8 * b; }
 };
+
+// Step it's buffer and the parity of its buffer barriers' completion for it.
+__device__ __forceinline__ int sbuf(int it) { return it % kSBufs; }
+__device__ __forceinline__ uint32_t spar(int it) { return static_cast<uint32_t>(it / kSBufs) & 1u; }
 
 // Bounded wait: true when the phase completed; false if this CTA is aborting
 // or the wait ran past the limit (then the failure is recorded).
@@ -287,9 +299,9 @@ __device__ __forceinline__ void issue_kmaj(uint32_t d_tmem, uint64_t a, uint64_t
 }
 
 // Issuer A: S^T and dP^T, the threads' operands.  Order:
-//   before the loop:  S^T(0)  dP^T(0)  S^T(1)
-//   step it:          [the threads have read dP^T(it)]  dP^T(it+1)
-//                     [dK(it) has read buffer it % 2]   S^T(it+2) into it
+//   before the loop:  S^T(0)  dP^T(0)  S^T(1)  S^T(2)
+//   step it:          [the threads have read dP^T(it)]          dP^T(it+1)
+//                     [the drain has read dQ^T(it-1), buffer]   S^T(it+2) into it
 // A stage is released by both issuers: by A after its dP^T, by B after its dK.
 template <int D>
 __device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const Sync& sy, const BwdParams& p, int n) {
@@ -301,13 +313,13 @@ __device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const S
   };
   const Desc<D> ds(sbase);
   wait_voted(sy.kv_full, 0);
-  auto issue_s_step = [&](int step) {  // S^T(step) into buffer step % 2, once its stage is in
+  auto issue_s_step = [&](int step) {  // S^T(step) into its buffer, once its stage is in
     wait_voted(sy.stage_full(step % C::kStages), (step / C::kStages) & 1);
     if (!ok) return;
     tc_fence_after_sync();
     if (leader) {
-      issue_kmaj<D>(tmem + kColS + (step & 1) * 64, ds.k_kmaj, ds.q_kmaj(step % C::kStages));
-      umma_commit(sy.s_full(step & 1));
+      issue_kmaj<D>(tmem + kColS + sbuf(step) * 64, ds.k_kmaj, ds.q_kmaj(step % C::kStages));
+      umma_commit(sy.s_full(sbuf(step)));
     }
     __syncwarp();
   };
@@ -323,7 +335,7 @@ __device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const S
   if (n > 0) {
     issue_s_step(0);
     if (ok) issue_dp_step(0);
-    if (n > 1 && ok) issue_s_step(1);
+    for (int step = 1; step < kSBufs && step < n && ok; ++step) issue_s_step(step);
   }
   for (int it = 0; it < n && ok; ++it) {
     if (it + 1 < n) {
@@ -331,10 +343,11 @@ __device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const S
       if (!ok) break;
       issue_dp_step(it + 1);
     }
-    if (it + 2 < n) {
-      wait_voted(sy.s_free(it & 1), (it >> 1) & 1);  // dV(it), dK(it) have read buffer it % 2
+    const int next = it + kSBufs - 1;  // the S^T that goes into step it-1's buffer
+    if (it >= 1 && next < n) {
+      wait_voted(sy.dq_free(sbuf(it - 1)), spar(it - 1));  // the drain has read dQ^T(it-1)
       if (!ok) break;
-      issue_s_step(it + 2);
+      issue_s_step(next);
     }
   }
   if (leader) umma_commit(sy.a_done);
@@ -343,7 +356,8 @@ __device__ __forceinline__ void run_mma_a(uint32_t sbase, uint32_t tmem, const S
 }
 
 // Issuer B: the products of the threads' step it, once its P^T and dS^T are
-// in: dV(it), dK(it), then dQ^T(it) once the drain has read dQ^T(it-1).
+// in: dV(it), dK(it), then dQ^T(it) into the same buffer (in issue order, so
+// after dV and dK have read P^T and dS^T there).
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Sync& sy,
                                         const BwdParams& p, int n) {
@@ -354,16 +368,15 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
     ok = __all_sync(0xffffffffu, ok && wait_phase(bar, par, sy, p, kSiteMma));
   };
   const Desc<D> ds(sbase);
-  const uint32_t tm_dq = tmem + kColDQ;
   const uint32_t tm_dv = tmem + kColDV, tm_dk = tmem + kColDK;
   constexpr uint32_t id_acc = idesc_bf16_f32_ab(kBlockK, D, false, true);      // dV, dK
   constexpr uint32_t id_dq = idesc_bf16_f32_ab(128, kBlockQ, true, true);      // dQ^T
   wait_voted(sy.kv_full, 0);
   for (int it = 0; it < n && ok; ++it) {
     const int st = it % C::kStages;
-    const int b = it & 1;
+    const int b = sbuf(it);
     const uint32_t tm_s = tmem + kColS + b * 64;
-    wait_voted(sy.sm_done(b), (it >> 1) & 1);  // P^T, dS^T of step it in
+    wait_voted(sy.sm_done(b), spar(it));  // P^T, dS^T of step it in
     if (!ok) break;
     tc_fence_after_sync();
     const uint32_t acc = it > 0 ? 1u : 0u;
@@ -374,17 +387,10 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
 #pragma unroll
       for (int kk = 0; kk < kBlockQ / 16; ++kk)  // dK += dS^T Q
         umma_ts(tm_dk, tm_s + 32 + kk * 8, sdesc_advance(ds.q_mn(st), kk * 2048), id_acc, kk > 0 ? 1u : acc);
-      umma_commit(sy.s_free(b));
       umma_commit(sy.stage_empty(st));  // B's last read of the stage
-    }
-    __syncwarp();
-    if (it > 0) wait_voted(sy.dq_free, (it - 1) & 1);  // the drain has read dQ^T(it-1)
-    if (!ok) break;
-    tc_fence_after_sync();
-    if (leader) {
 #pragma unroll
-      for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T
-        umma_ss(tm_dq, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
+      for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T, over P^T and dS^T
+        umma_ss(tm_s, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
                 kk > 0 ? 1u : 0u);
       umma_commit(sy.dq_full(b));
     }
@@ -413,10 +419,10 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
   const uint64_t qk2 = f2_pack(p.qk_scale, p.qk_scale);
   bool ok = true;
   for (int it = 0; it < n && ok; ++it) {
-    const int b = it & 1;
+    const int b = sbuf(it);
     const int st = it % C::kStages;
     const int q0 = (j0 + it) * kBlockQ;
-    bool w = wait_phase(sy.s_full(b), (it >> 1) & 1, sy, p, kSiteDs);
+    bool w = wait_phase(sy.s_full(b), spar(it), sy, p, kSiteDs);
     w = w && wait_phase(sy.stage_full(st), (it / C::kStages) & 1, sy, p, kSiteDs);  // L, D of the step
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
@@ -463,12 +469,12 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
 
     // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16, stored to tensor
     // memory after P^T (the A operand of dK) and to the 128-byte-swizzled dS^T
-    // tile it % 2 in shared memory (the B operand of dQ^T; 16-byte chunk ch of
-    // row r at chunk ch ^ (r % 8)).
+    // tile b in shared memory (the B operand of dQ^T; 16-byte chunk ch of row
+    // r at chunk ch ^ (r % 8)).
     w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
-    // Tile it % 2 was last read by dQ^T(it-2): wait for that completion of
+    // Tile b was last read by dQ^T(it - kSBufs): wait for that completion of
     // its barrier (the next one, step it's, needs this warpgroup's step it).
-    if (it >= 2) w = w && wait_phase(sy.dq_full(b), ((it - 2) >> 1) & 1, sy, p, kSiteDs);
+    if (it >= kSBufs) w = w && wait_phase(sy.dq_full(b), spar(it - kSBufs), sy, p, kSiteDs);
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after_sync();
@@ -556,14 +562,15 @@ __device__ __forceinline__ void run_drain(uint32_t tmem, const Sync& sy, const B
   const bool has_rows = quad * 32 < D;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   for (int it = 0; it < n; ++it) {
-    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full(it & 1), (it >> 1) & 1, sy, p, kSiteDrain));
+    const int b = sbuf(it);
+    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full(b), spar(it), sy, p, kSiteDrain));
     if (!ok) break;
     tc_fence_after_sync();
     uint32_t x[kBlockQ];
-    tmem_ld64_wait(tmem + lane_off + kColDQ, x);
+    tmem_ld64_wait(tmem + lane_off + kColS + b * 64, x);
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) mbar_arrive(sy.dq_free);
+    if (lane == 0) mbar_arrive(sy.dq_free(b));
     if (!has_rows) continue;
     const int q0 = (j0 + it) * kBlockQ;
     const int rows = min(kBlockQ, p.Nq - q0);
@@ -614,16 +621,15 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     sy.stage_empty0 = next();
     for (int i = 1; i < C::kStages; ++i) next();
     sy.s_full0 = next();
-    next();
-    sy.s_free0 = next();
-    next();
+    for (int i = 1; i < kSBufs; ++i) next();
+    sy.sm_done0 = next();
+    for (int i = 1; i < kSBufs; ++i) next();
+    sy.dq_full0 = next();
+    for (int i = 1; i < kSBufs; ++i) next();
+    sy.dq_free0 = next();
+    for (int i = 1; i < kSBufs; ++i) next();
     sy.dp_full = next();
     sy.dp_read = next();
-    sy.sm_done0 = next();
-    next();
-    sy.dq_full0 = next();
-    next();
-    sy.dq_free = next();
     sy.acc_done = next();
     sy.a_done = next();
   }
@@ -636,15 +642,14 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_init(sy.stage_full(i), 1);
       mbar_init(sy.stage_empty(i), 2);  // released by both issuers
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(sy.s_full(i), 1);
-      mbar_init(sy.s_free(i), 1);
       mbar_init(sy.sm_done(i), 4);  // one arrival per P / dS warp
       mbar_init(sy.dq_full(i), 1);
+      mbar_init(sy.dq_free(i), 4);  // one arrival per drain warp
     }
     mbar_init(sy.dp_full, 1);
     mbar_init(sy.dp_read, 4);  // one arrival per P / dS warp
-    mbar_init(sy.dq_free, 4);  // one arrival per drain warp
     mbar_init(sy.acc_done, 1);
     mbar_init(sy.a_done, 1);
     *sy.abort_flag = 0;
