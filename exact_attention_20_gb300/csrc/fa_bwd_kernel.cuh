@@ -24,8 +24,10 @@
 //   dQ^T = K^T dS^T   M = d (128 lanes), N = 64 queries, K = 128 keys (dS^T
 //                     read from shared memory)
 // Every key block adds to every query row's dQ, so each step's dQ^T is added
-// into an fp32 accumulator in global memory by reductions from registers
-// (red.global.add: the adds are done in L2).  With d = 64 the dQ^T product
+// into an fp32 accumulator in global memory: the drain warps write it to a
+// shared-memory tile (64 query rows of d values, the accumulator's own row
+// layout) and one bulk reduction adds the tile to the step's rows, the adds
+// done in L2.  With d = 64 the dQ^T product
 // still has M = 128: rows 64-127 of its A operand are V^T (the tile that
 // follows K in shared memory) and those lanes are ignored.
 //
@@ -42,9 +44,9 @@
 // one per step in turn: a step's S^T, then its P^T and dS^T (bf16, the
 // first and the second 32 columns, written over S^T by the threads), then
 // its dQ^T (written once dV and dK have read P^T and dS^T); dP^T at 192, dV
-// at 256, dK at 384.  The dS^T tile in shared memory has three buffers too.
-// A buffer takes S^T again once the drain has read its dQ^T, so S^T runs up
-// to three steps ahead of the threads.
+// at 256, dK at 384.  The dS^T tile in shared memory has two buffers.  A
+// buffer takes S^T again once the drain has read its dQ^T, so S^T runs up to
+// three steps ahead of the threads.
 //
 // At M = 128 the tensor core takes an N = 64 instruction every 48 cycles and
 // accepts about one more than it is running, so an issuer that stops to wait
@@ -106,8 +108,10 @@ struct Cfg {
   static constexpr int kStageOff = kVOff + kKTile;
   static constexpr int kStageBytes = 2 * kQTile;  // Q, then dO
   static constexpr int kDsOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries], kSBufs tiles
-  static constexpr int kLdOff = kDsOff + kSBufs * kDsBytes;  // per stage: L[64] then D[64], fp32
+  static constexpr int kDsBytes = kBlockK * kBlockQ * 2;  // dS^T, bf16 [128 keys][64 queries], two tiles
+  static constexpr int kDqOff = kDsOff + 2 * kDsBytes;    // dQ of a step, fp32 [64 queries][D], for the reduction
+  static constexpr int kDqBytes = kBlockQ * D * 4;
+  static constexpr int kLdOff = kDqOff + kDqBytes;        // per stage: L[64] then D[64], fp32
   static constexpr int kLdBytes = 2 * kBlockQ * 4;
   static constexpr int kBarOff = kLdOff + kStages * kLdBytes;
   static constexpr int kNumBars = 11 + 4 * kSBufs + 2 * kStages;
@@ -141,9 +145,9 @@ struct BwdParams {
 // Buffer barriers complete once every kSBufs steps:
 //   s_full(b)   S^T of a step in buffer b
 //   sm_done(b)  the threads' P^T, dS^T of a step in buffer b are in, and its
-//               dS^T tile b in shared memory
-//   dq_full(b)  dQ^T of a step in buffer b: the drain reads it, and dS^T
-//               tile b may be written again
+//               dS^T tile in shared memory
+//   dq_full(b)  dQ^T of a step in buffer b: the drain reads it, and the
+//               step's dS^T tile (step % 2) may be written again
 //   dq_free(b)  the drain has read it: buffer b may take S^T again
 // and once per step:
 //   dp_full     dP^T of a step in tensor memory
@@ -390,7 +394,7 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
       umma_commit(sy.stage_empty(st));  // B's last read of the stage
 #pragma unroll
       for (int kk = 0; kk < kBlockK / 16; ++kk)  // dQ^T = K^T dS^T, over P^T and dS^T
-        umma_ss(tm_s, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(b), kk * 2048), id_dq,
+        umma_ss(tm_s, sdesc_advance(ds.kt_mn, kk * 2048), sdesc_advance(ds.ds_mn(it & 1), kk * 2048), id_dq,
                 kk > 0 ? 1u : 0u);
       umma_commit(sy.dq_full(b));
     }
@@ -469,12 +473,13 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
 
     // dS^T row: ds_c = p_c * (dP_c - D_c), rounded to bf16, stored to tensor
     // memory after P^T (the A operand of dK) and to the 128-byte-swizzled dS^T
-    // tile b in shared memory (the B operand of dQ^T; 16-byte chunk ch of row
-    // r at chunk ch ^ (r % 8)).
+    // tile it % 2 in shared memory (the B operand of dQ^T; 16-byte chunk ch of
+    // row r at chunk ch ^ (r % 8)).
     w = wait_phase(sy.dp_full, it & 1, sy, p, kSiteDs);
-    // Tile b was last read by dQ^T(it - kSBufs): wait for that completion of
-    // its barrier (the next one, step it's, needs this warpgroup's step it).
-    if (it >= kSBufs) w = w && wait_phase(sy.dq_full(b), spar(it - kSBufs), sy, p, kSiteDs);
+    // The tile was last read by dQ^T(it-2): wait for that completion of its
+    // buffer's barrier (the next one, step it+1's, needs this warpgroup's step
+    // it+1).
+    if (it >= 2) w = w && wait_phase(sy.dq_full(sbuf(it - 2)), spar(it - 2), sy, p, kSiteDs);
     ok = __all_sync(0xffffffffu, w);
     if (!ok) break;
     tc_fence_after_sync();
@@ -484,7 +489,7 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
     tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) mbar_arrive(sy.dp_read);
-    uint8_t* ds_row = smem + C::kDsOff + b * C::kDsBytes + r * 128;
+    uint8_t* ds_row = smem + C::kDsOff + (it & 1) * C::kDsBytes + r * 128;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t wds[16];
@@ -549,41 +554,59 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
 // ---------------------------------------------------------------------------
 // dQ drain (warps 8-11): thread = one row of dQ^T (one column of d)
 // ---------------------------------------------------------------------------
-// Per step each thread adds its 64 values of dQ^T (one column of d, 64 query
-// rows) into the fp32 accumulator, one reduction per query row: a warp's
-// reduction covers 32 consecutive floats (128 bytes) of one row.  Rows past
-// the last query are skipped.  With d = 64 only warps 8 and 9 hold dQ^T rows.
+// Per step each thread writes its 64 values of dQ^T (one column of d, 64
+// query rows) into the shared-memory tile in the accumulator's row layout (a
+// warp's store covers 32 consecutive floats of one row), and one thread adds
+// the tile's rows below Nq to the accumulator with one bulk reduction.  The
+// tile is written again once that reduction has read it.  With d = 64 only
+// warps 8 and 9 hold dQ^T rows.
+constexpr uint32_t kDrainBar = 1;  // named barrier of the four drain warps
+
 template <int D>
-__device__ __forceinline__ void run_drain(uint32_t tmem, const Sync& sy, const BwdParams& p, int bh, int j0,
-                                          int n) {
+__device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t tmem, const Sync& sy, const BwdParams& p, int bh,
+                                          int j0, int n) {
+  using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quad = warp & 3;
   const bool has_rows = quad * 32 < D;
+  const bool issuer = warp == kDrainWarp0 && lane == 0;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  float* tile = reinterpret_cast<float*>(smem + C::kDqOff) + quad * 32 + lane;
+  // Every drain warp runs all n steps and takes both named barriers of each,
+  // whatever its waits returned, so the barriers never wait for a warp that
+  // has left; after a failed wait (the CTA is aborting) a warp only skips the
+  // work, and the reduction is not issued.
+  bool ok = true;
   for (int it = 0; it < n; ++it) {
     const int b = sbuf(it);
-    const bool ok = __all_sync(0xffffffffu, wait_phase(sy.dq_full(b), spar(it), sy, p, kSiteDrain));
-    if (!ok) break;
-    tc_fence_after_sync();
+    const bool w = __all_sync(0xffffffffu, ok && wait_phase(sy.dq_full(b), spar(it), sy, p, kSiteDrain));
+    ok = w;
     uint32_t x[kBlockQ];
-    tmem_ld64_wait(tmem + lane_off + kColS + b * 64, x);
-    tc_fence_before_sync();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sy.dq_free(b));
-    if (!has_rows) continue;
-    const int q0 = (j0 + it) * kBlockQ;
-    const int rows = min(kBlockQ, p.Nq - q0);
-    float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + q0) * D + quad * 32 + lane;
-    if (rows == kBlockQ) {
+    if (w) {
+      tc_fence_after_sync();
+      tmem_ld64_wait(tmem + lane_off + kColS + b * 64, x);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sy.dq_free(b));
+    }
+    if (issuer && it > 0) tma_store_wait_read0();  // the last reduction has read the tile
+    named_bar_sync(kDrainBar, 128);
+    if (w && has_rows) {
 #pragma unroll
-      for (int c = 0; c < kBlockQ; ++c) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(x[c]));
-    } else {
-#pragma unroll
-      for (int c = 0; c < kBlockQ; ++c)
-        if (c < rows) red_add_f32(dst + static_cast<size_t>(c) * D, __uint_as_float(x[c]));
+      for (int c = 0; c < kBlockQ; ++c) tile[c * D] = __uint_as_float(x[c]);
+    }
+    fence_proxy_async_smem();  // the tile is visible to the bulk reduction
+    named_bar_sync(kDrainBar, 128);
+    if (issuer && w && !*sy.abort_flag) {
+      const int q0 = (j0 + it) * kBlockQ;
+      const int rows = min(kBlockQ, p.Nq - q0);
+      bulk_reduce_add_f32(p.dq_acc + (static_cast<size_t>(bh) * p.Nq + q0) * D, smem_u32(smem + C::kDqOff),
+                          static_cast<uint32_t>(rows * D * 4));
+      tma_store_commit();
     }
   }
+  if (issuer) tma_store_wait_all0();  // every reduction is done before the CTA exits
 }
 
 // ---------------------------------------------------------------------------
@@ -680,7 +703,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else if (warp >= kDsWarp0 && warp < kDsWarp0 + 4) {
     run_ds<D, CAUSAL>(smem, tmem, sy, p, bh, kb, j0, n);
   } else if (warp >= kDrainWarp0) {
-    run_drain<D>(tmem, sy, p, bh, j0, n);
+    run_drain<D>(smem, tmem, sy, p, bh, j0, n);
   }
 
   tc_fence_before_sync();
