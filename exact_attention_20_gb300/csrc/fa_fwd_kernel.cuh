@@ -254,39 +254,6 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // ---------------------------------------------------------------------------
 // TMA producer (one thread)
 // ---------------------------------------------------------------------------
-// Steps before a chunk's end at which the next chunk's first tiles are
-// prefetched into L2 (the producer runs about half the ring ahead of the
-// tensor core, so this is several steps of work before they are needed).
-constexpr int kPrefetchSteps = 2;
-
-// L2 prefetch of chunk q's Q tiles and its first step's K and V tiles
-// (boxes past the end of a tensor are not fetched).
-template <int D, bool CAUSAL, int E, bool PAIRED>
-__device__ __forceinline__ void prefetch_chunk(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                               int q, const WorkRange& wr, const SlotPair& sp, const FwdParams& p) {
-  using C = Cfg<D, E>;
-  const int item = chunk_item(q, wr);
-  int rb, bh;
-  decode_item(item, p, rb, bh);
-  const Chunk ch = chunk_of(item, item_steps<CAUSAL, PAIRED>(rb, p), wr, sp, p);
-  for (int t = 0; t < kQTiles; ++t) {
-    if (min(ch.ke, tiles_for<CAUSAL, PAIRED>(rb, t, p)) <= ch.kb) continue;
-#pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmQ, s * (128 / E), tile_row0(rb, t, PAIRED), tile_head(bh, t, PAIRED));
-  }
-  for (int h = 0; h < (PAIRED ? 2 : 1); ++h) {
-    const int head = PAIRED ? 2 * bh + h : bh;
-#pragma unroll
-    for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmK, s * (128 / E), ch.kb * kBlockN, head);
-    if (E == 1) {
-      tma_prefetch_3d(tmV, ch.kb * kBlockN, 0, head);
-    } else {
-#pragma unroll
-      for (int s = 0; s < C::kSlabs; ++s) tma_prefetch_3d(tmV, s * (128 / E), ch.kb * kBlockN, head);
-    }
-  }
-}
-
 template <int D, bool CAUSAL, int E = 2, bool PAIRED = false>
 __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              uint32_t sbase, const Sync& sy, const FwdParams& p) {
@@ -333,12 +300,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tmQ, const CUten
     if (p.starve_kv) continue;  // self-test: never deliver K/V
     // per step: K then V (normal), or K of both heads then V of both (paired)
     const int heads = PAIRED ? 2 : 1;
-    // A few steps before the chunk ends (at its start if it is short), the
-    // next chunk's Q tiles and first K, V tiles are brought into L2, so that
-    // their loads at the boundary are not DRAM round trips.
-    const int j_prefetch = max(ch.kb, ch.ke - kPrefetchSteps);
     for (int j = ch.kb; j < ch.ke && ok; ++j) {
-      if (j == j_prefetch && q + 1 < nq) prefetch_chunk<D, CAUSAL, E, PAIRED>(tmQ, tmK, tmV, q + 1, wr, sp, p);
 #pragma unroll
       for (int n = 0; n < 2 * heads; ++n) {
         if (!ok) break;
