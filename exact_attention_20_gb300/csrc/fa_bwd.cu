@@ -86,7 +86,8 @@ int check_bwd_args(const void* q, const void* k, const void* v, const void* o, c
   const long long BH = static_cast<long long>(B) * H;
   const long long nq_pad = (static_cast<long long>(Nq) + 63) / 64 * 64;
   if (BH * nq_pad * d >= (1ll << 31) || BH * Nk * d >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-  if (BH > 65535) return FA_ERR_INVALID_ARG;  // the grid's y dimension
+  if (BH > 65535) return FA_ERR_INVALID_ARG;  // the grid's y dimension without the mask
+  if (causal && (static_cast<long long>(Nk) + 127) / 128 > 65535) return FA_ERR_INVALID_ARG;  // ... with it
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_NULL;
   auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   for (const void* p : {q, k, v, o, dout, dq, dk, dv})
@@ -162,7 +163,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.scale = scale;
   p.wait_limit_ns = fa_internal::kWaitLimitNs;
   fa::bwd::fa_bwd_kernel<D, CAUSAL>
-      <<<dim3(n_kb, BH), fa::bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+      <<<CAUSAL ? dim3(BH, n_kb) : dim3(n_kb, BH), fa::bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
 
   const long long n8 = static_cast<long long>(BH) * Nq * D / 8;

@@ -610,8 +610,12 @@ __device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t tmem, const Sy
 }
 
 // ---------------------------------------------------------------------------
-// Kernel: grid (key blocks, B*H).  The CTAs of one head are adjacent in launch
-// order, so the ones running together share their heads' Q and dO tiles in L2.
+// Kernel: grid (key blocks, B*H) without the mask: the CTAs of one head are
+// adjacent in launch order, so the ones running together share their heads'
+// Q and dO tiles in L2.  Under the causal mask a key block's work falls with
+// its index (block kb walks the query rows from kb * 128 on), so the grid is
+// (B*H, key blocks): every head's first key block, the longest, is launched
+// first and the shortest last, and the last wave holds short blocks only.
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -627,8 +631,8 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kb = blockIdx.x;
-  const int bh = blockIdx.y;
+  const int kb = CAUSAL ? blockIdx.y : blockIdx.x;
+  const int bh = CAUSAL ? blockIdx.x : blockIdx.y;
   // Query steps of this key block: under the top-left causal mask key j is
   // seen by queries i >= j, so the first step is the one holding query kb*128.
   const int j0 = CAUSAL ? (kb * kBlockK) / kBlockQ : 0;

@@ -196,7 +196,8 @@ int fa_fwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int* num_ctas,
  *   dk, dv     : bf16 [B][H][Nk][d]; written.  No output may overlap an input or another output.
  *   B, H, Nq, Nk, d, causal, scale : as for fa_fwd_rect (the same values the
  *             forward used; causal is the top-left mask), with
- *             B*H*ceil(Nq/64)*64*d < 2^31, B*H*Nk*d < 2^31 and B*H <= 65535.
+ *             B*H*ceil(Nq/64)*64*d < 2^31, B*H*Nk*d < 2^31, B*H <= 65535 and,
+ *             with causal = 1, ceil(Nk/128) <= 65535.
  *   stream     : cudaStream_t as void*.
  *
  * The method is the recompute-from-L backward of "FlashAttention and

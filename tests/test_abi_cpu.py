@@ -192,6 +192,8 @@ def test_bwd_entry_checks_arguments(fa):
     assert call(*args, scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert call(*args, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
     assert call(*args, B=65536, H=1, Nq=1, Nk=1) == fa.FA_ERR_INVALID_ARG   # more heads than the grid takes
+    # with the mask the key blocks take the grid's y dimension: at most 65535 of 128 keys
+    assert call(*args, B=1, H=1, Nq=1, Nk=65535 * 128 + 1, causal=1) == fa.FA_ERR_INVALID_ARG
     for i in range(9):
         bad = list(args)
         bad[i] = None
