@@ -94,9 +94,10 @@ def test_batch_head_indexing(fa, B, H, N, d, causal):
 # Keys of 1.5 in the last tile raise each row's maximum there by about 20
 # (d = 128) or 10 (d = 64) log2 units: below the bf16 path's rescale threshold
 # of 32, so P grows past 1 against the old reference and nothing is rescaled.
-# Keys of 5.0 raise it by about 65 or 46: the reference moves, the tile is
-# exponentiated again and the accumulator rescaled.
-@pytest.mark.parametrize("k_last", [1.5, 5.0])
+# Keys of 5.0 raise it by about 65 or 46 and keys of 8.0 by about 105 or 74:
+# the reference moves, the tile is exponentiated again and the accumulator
+# rescaled.
+@pytest.mark.parametrize("k_last", [1.5, 5.0, 8.0])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_max_in_last_key_tile(fa, d, causal, k_last):
@@ -111,7 +112,7 @@ def test_max_in_last_key_tile(fa, d, causal, k_last):
     assert_close(compare(o, lse, *oracle_full(q, k, v, d ** -0.5, causal)), "max-last")
 
 
-@pytest.mark.parametrize("k_last", [1.5, 5.0])
+@pytest.mark.parametrize("k_last", [1.5, 5.0, 8.0])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_max_jumps_in_some_rows_only(fa, d, causal, k_last):
