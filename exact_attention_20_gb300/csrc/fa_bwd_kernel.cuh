@@ -37,9 +37,9 @@
 //              TMEM allocation
 //   warp 2     MMA issuer A (one lane issues): S^T, dP^T
 //   warp 3     idle
-//   warps 4-7  P and dS, one key row per thread; the dK, dV epilogue
+//   warps 4-7  P and dS, one key row per thread; then dV of the row
 //   warps 8-11 dQ drain: one row of dQ^T (a column of d) per thread, reduced
-//              into the fp32 accumulator
+//              into the fp32 accumulator; then scale * dK of a key row
 // Tensor memory (32-bit columns): three 64-column buffers at 0, 64 and 128,
 // one per step in turn: a step's S^T, then its P^T and dS^T (bf16, the
 // first and the second 32 columns, written over S^T by the threads), then
@@ -410,8 +410,37 @@ __device__ __forceinline__ void run_mma(uint32_t sbase, uint32_t tmem, const Syn
   mbar_wait_bounded(sy.acc_done, 0, p.wait_limit_ns);
 }
 
+// mul * (an accumulator row of d fp32 values in tensor memory, from column
+// address t) to key row `key` of dst [BH][Nk][D] in bf16, if key < Nk.  A
+// block with no visible query row (causal, keys past the last query: n = 0)
+// writes zeros.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t t, __nv_bfloat16* dst, float mul, int bh, int key, int Nk,
+                                              int n) {
+  const bool store = key < Nk;
+  uint4* out = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * Nk + key) * D);
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t a[32];
+    if (n > 0) {
+      tmem_ld32_wait(t + c0, a);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+    if (store) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[c0 / 8 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
-// P and dS (warps 4-7, one key row per thread), then the dK, dV epilogue
+// P and dS (warps 4-7, one key row per thread), then the dV epilogue
 // ---------------------------------------------------------------------------
 template <int D, bool CAUSAL>
 __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync& sy,
@@ -522,39 +551,12 @@ __device__ __forceinline__ void run_ds(uint8_t* smem, uint32_t tmem, const Sync&
     if (lane == 0) mbar_arrive(sy.sm_done(b));
   }
 
-  // Epilogue: dV and scale * dK of this thread's key row, bf16.  A block with
-  // no visible query row (causal, keys past the last query) writes zeros.
+  // Epilogue: dV of this thread's key row (the drain warps write dK).
   bool w = wait_phase(sy.acc_done, 0, sy, p, kSiteDs);
   ok = __all_sync(0xffffffffu, ok && w);
   if (!ok || *sy.abort_flag) return;
   tc_fence_after_sync();
-  const bool store = key < p.Nk;
-  const size_t row_off = (static_cast<size_t>(bh) * p.Nk + key) * D;
-#pragma unroll 1
-  for (int which = 0; which < 2; ++which) {
-    __nv_bfloat16* dst = (which == 0 ? p.dv : p.dk) + row_off;
-    const float mul = which == 0 ? 1.f : p.scale;
-    const uint32_t col = which == 0 ? kColDV : kColDK;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t a[32];
-      if (n > 0) {
-        tmem_ld32_wait(tmem + lane_off + col + c0, a);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = 0u;
-      }
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
-      if (store) {
-        uint4* out = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-      }
-    }
-  }
+  store_acc_row<D>(tmem + lane_off + kColDV, p.dv, 1.f, bh, key, p.Nk, n);
 }
 
 // ---------------------------------------------------------------------------
@@ -570,7 +572,7 @@ constexpr uint32_t kDrainBar = 1;  // named barrier of the four drain warps
 
 template <int D>
 __device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t tmem, const Sync& sy, const BwdParams& p, int bh,
-                                          int j0, int n) {
+                                          int kb, int j0, int n) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -612,7 +614,17 @@ __device__ __forceinline__ void run_drain(uint8_t* smem, uint32_t tmem, const Sy
       tma_store_commit();
     }
   }
-  if (issuer) tma_store_wait_all0();  // every reduction is done before the CTA exits
+
+  // Epilogue: scale * dK of key row quad * 32 + lane, while the last
+  // reductions run.
+  const bool w = wait_phase(sy.acc_done, 0, sy, p, kSiteDrain);
+  if (__all_sync(0xffffffffu, ok && w) && !*sy.abort_flag) {
+    tc_fence_after_sync();
+    store_acc_row<D>(tmem + lane_off + kColDK, p.dk, p.scale, bh, kb * kBlockK + quad * 32 + lane, p.Nk, n);
+  }
+  // The tile must stay in place until every reduction has read it; the
+  // adds themselves are complete when the kernel is.
+  if (issuer) tma_store_wait_read0();
 }
 
 // ---------------------------------------------------------------------------
@@ -710,7 +722,7 @@ fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   } else if (warp >= kDsWarp0 && warp < kDsWarp0 + 4) {
     run_ds<D, CAUSAL>(smem, tmem, sy, p, bh, kb, j0, n);
   } else if (warp >= kDrainWarp0) {
-    run_drain<D>(smem, tmem, sy, p, bh, j0, n);
+    run_drain<D>(smem, tmem, sy, p, bh, kb, j0, n);
   }
 
   tc_fence_before_sync();
