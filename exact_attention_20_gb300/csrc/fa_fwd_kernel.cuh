@@ -450,9 +450,17 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       const uint32_t ck = kv_count + kvps * (s - kb) + koff;      // K_s
       // K/V (landed long before, as a rule) first, then the descriptors, and
       // the softmax's P last: once P is in, only the turn stands between it
-      // and the products.
-      if (do_pv) wait_full(cv);
-      if (do_s) wait_full(ck);
+      // and the products.  A full barrier's wait is by parity: it tells fill
+      // n of a slot from fill n-1 only, so the waiter must know that fill n-1
+      // is complete.  Without pairing both issuers wait for every position of
+      // the ring, in order, which guarantees it.  With pairing a slot's
+      // consecutive fills go to different tiles' K and V, and the fill before
+      // this issuer's was waited for by the other issuer in its previous
+      // group: this issuer waits for its K/V only once it has the turn, that
+      // is once that group is issued (before, it could take the earlier fill,
+      // still being loaded, for its own).
+      if (!PAIRED && do_pv) wait_full(cv);
+      if (!PAIRED && do_s) wait_full(ck);
       uint64_t dv[C::kPvInstr], dq[C::kQkInstr], dk[C::kQkInstr];
       {
         const uint64_t v0 = sdesc_advance(v_desc0, (cv % C::kStages) * C::kTileBytes);
@@ -481,6 +489,8 @@ __device__ __forceinline__ void run_mma(int t, uint32_t sbase, uint32_t tmem, co
       // that the turn holds only the MMA instructions themselves.
       wait_voted(my_turn, turn_par);
       turn_par ^= 1u;
+      if (PAIRED && do_pv) wait_full(cv);
+      if (PAIRED && do_s) wait_full(ck);
       if (!ok) break;
       tc_fence_after_sync();
       if (leader) {

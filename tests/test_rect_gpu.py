@@ -84,6 +84,29 @@ def test_rect_paired_heads(fa, d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_rect_paired_heads_repeated(fa, causal):
+    # The K/V ring's slots take the two paired heads' tiles in turn, so an
+    # issuer that waited for its tile before the other one had seen the
+    # slot's previous fill could read that previous tile (one head's output
+    # wrong in some launches, depending on load timing).  100 launches of the
+    # paired shape on the same inputs: the first against the oracle, every
+    # other one against the first (merge order may move the last bits).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    H = 2 * sms + 16
+    q, k, v = _inputs(1, H, 100, 1000, 128, seed=43)
+    scale = 128 ** -0.5
+    o0, lse0 = fa.attention_rect(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert_close(compare(o0, lse0, *_oracle(q, k, v, scale, causal)), f"paired heads causal={causal}")
+    worst_o, worst_l = 0.0, 0.0
+    for _ in range(100):
+        o, lse = fa.attention_rect(q, k, v, causal=causal, scale=scale)
+        worst_o = max(worst_o, (o.float() - o0.float()).abs().max().item())
+        worst_l = max(worst_l, (lse - lse0).abs().max().item())
+    assert worst_o <= 1e-2 and worst_l <= 1e-3, (worst_o, worst_l)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_rect_square_is_fa_fwd(fa, causal):
     q, k, v = make_qkv(2, 3, 777, 128, seed=41, device=DEV)
     o1, l1 = fa.attention(q, k, v, causal=causal)
