@@ -83,8 +83,9 @@ def test_rect_paired_heads(fa, d, causal):
     assert_close(compare(o, lse, *_oracle(q, k, v, scale, causal)), f"paired heads d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_rect_paired_heads_repeated(fa, causal):
+def test_rect_paired_heads_repeated(fa, d, causal):
     # The K/V ring's slots take the two paired heads' tiles in turn, so an
     # issuer that waited for its tile before the other one had seen the
     # slot's previous fill could read that previous tile (one head's output
@@ -93,11 +94,11 @@ def test_rect_paired_heads_repeated(fa, causal):
     # other one against the first (merge order may move the last bits).
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     H = 2 * sms + 16
-    q, k, v = _inputs(1, H, 100, 1000, 128, seed=43)
-    scale = 128 ** -0.5
+    q, k, v = _inputs(1, H, 100, 1000, d, seed=43)
+    scale = d ** -0.5
     o0, lse0 = fa.attention_rect(q, k, v, causal=causal, scale=scale)
     torch.cuda.synchronize()
-    assert_close(compare(o0, lse0, *_oracle(q, k, v, scale, causal)), f"paired heads causal={causal}")
+    assert_close(compare(o0, lse0, *_oracle(q, k, v, scale, causal)), f"paired heads d={d} causal={causal}")
     worst_o, worst_l = 0.0, 0.0
     for _ in range(100):
         o, lse = fa.attention_rect(q, k, v, causal=causal, scale=scale)
