@@ -51,36 +51,42 @@ class Barrier:
         return (self.completed & 1) != parity
 
 
-def run(ring, paired, wait_after_turn, steps, rng):
-    """One random schedule.  Returns (stale_waits, finished)."""
+def run(ring, paired, wait_after_turn, chunks, rng):
+    """One random schedule over chunks of the given step counts (a CTA's
+    items, or parts of items, in turn).  Returns (stale_waits, finished)."""
     heads = 2 if paired else 1
     per_step = 2 * heads                     # K of each head, then V of each
-    n_pos = per_step * steps
+    n_pos = per_step * sum(chunks)
+    # every issuer walks the same groups: chunk c's groups s = 0 .. chunks[c],
+    # group s reading V(s-1) and K(s) of the chunk
+    groups = [(c, s) for c in range(len(chunks)) for s in range(chunks[c] + 1)]
+    base = [per_step * sum(chunks[:c]) for c in range(len(chunks))]
     full = [Barrier(1) for _ in range(ring)]
     empty = [Barrier(2) for _ in range(ring)]  # two releases per fill either way
 
-    def pos_k(t, s):
-        return per_step * s + (t if paired else 0)
+    def pos_k(t, c, s):
+        return base[c] + per_step * s + (t if paired else 0)
 
-    def pos_v(t, s):
-        return per_step * s + heads + (t if paired else 0)
+    def pos_v(t, c, s):
+        return base[c] + per_step * s + heads + (t if paired else 0)
 
     # producer state
     prod_next = 0
     loads_in_flight = []                     # positions whose fill has not landed
-    # issuer state: the groups s = 0 .. steps (group s reads V(s-1) and K(s))
+    # issuer state: index into `groups`
     group = [0, 0]
     kv_idx = [0, 0]                          # the group's K/V waits passed so far
     turn = 0
     mma_in_flight = []                       # (tile, positions) whose products have not completed
     stale = 0
 
-    def needs(t, s):
+    def needs(t, g):
+        c, s = groups[g]
         ps = []
         if s >= 1:
-            ps.append(pos_v(t, s - 1))
-        if s < steps:
-            ps.append(pos_k(t, s))
+            ps.append(pos_v(t, c, s - 1))
+        if s < chunks[c]:
+            ps.append(pos_k(t, c, s))
         return ps
 
     def kv_done(t):
@@ -110,7 +116,7 @@ def run(ring, paired, wait_after_turn, steps, rng):
         if mma_in_flight:
             actions.append("mma_done")
         for t in (0, 1):
-            if group[t] > steps:
+            if group[t] == len(groups):
                 continue
             if not kv_done(t) and (not wait_after_turn or turn == t) and kv_ready(t):
                 actions.append(("kv", t))
@@ -138,16 +144,16 @@ def run(ring, paired, wait_after_turn, steps, rng):
             group[t] += 1
             kv_idx[t] = 0
             turn = 1 - t
-    finished = group[0] > steps and group[1] > steps and prod_next == n_pos
+    finished = group[0] == len(groups) and group[1] == len(groups) and prod_next == n_pos
     return stale, finished
 
 
-def sweep(ring, paired, wait_after_turn, runs=300, steps=12, seed=0):
+def sweep(ring, paired, wait_after_turn, runs=300, chunks=(12,), seed=0):
     """(stale waits, schedules that stopped before the end) over random schedules."""
     rng = random.Random(seed)
     stale = stopped = 0
     for _ in range(runs):
-        s, finished = run(ring, paired, wait_after_turn, steps, rng)
+        s, finished = run(ring, paired, wait_after_turn, list(chunks), rng)
         stale += s
         stopped += not finished
     return stale, stopped
@@ -173,3 +179,13 @@ def test_paired_waits_before_the_turn_can_take_a_stale_fill():
 @pytest.mark.parametrize("ring", [6, 7, 9, 13])
 def test_paired_waits_before_the_turn_are_sound_from_six_slots(ring):
     assert sweep(ring, paired=True, wait_after_turn=False) == (0, 0)
+
+
+@pytest.mark.parametrize("chunks", [(1, 1, 1, 1, 1, 1), (3, 8, 2), (5, 1, 7)])
+@pytest.mark.parametrize("ring", [5, 9])
+def test_chunk_boundaries(ring, chunks):
+    # a CTA's chunks in turn (the first and last group of a chunk read one
+    # tile each); paired items under the causal mask with at most 128 rows
+    # take one step each
+    assert sweep(ring, paired=False, wait_after_turn=False, runs=150, chunks=chunks) == (0, 0)
+    assert sweep(ring, paired=True, wait_after_turn=True, runs=150, chunks=chunks) == (0, 0)
